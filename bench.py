@@ -1,0 +1,428 @@
+"""Benchmark of paged GQA decode (headline) and selected-sparse prefill.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Headline workload: long-context FP8-E4M3 decode, B=16, Hkv=4, Hq=24 (GQA-6),
+D=256, seq_lens uniform in [12288, 16384], page size 16, a shuffled pool of
+16384 pages.  One step = one decode pass over the batch (split kernel + LSE
+merge kernel).  ``value`` = algorithmic KV bytes read per step (sum_b L_b *
+Hkv * D * 2 * 1 byte) x K / time, in GB/s; decode tok/s = B / step time.
+The L2 (129 MB) is flushed between steps by writing a 256 MB buffer outside
+the timed events, and the KV bytes per step (~470 MB) exceed L2 as well.
+
+The same line reports the selected-sparse prefill (4096 rows, 512 selected
+four-token blocks + a 1..3-token tail, Hq6/Hkv1/D256 FP16, interleaved K/V,
+32768-token cache) timed the same way, the roofline of the dominant kernel
+(the decode split kernel, timed by CUDA events the library records around it
+on the launching stream), an end-to-end number through host buffers, SM
+clocks sampled during the timed phases, and the FP64 CPU oracle timed on a
+bounded sample as a baseline.
+
+``--impl reference`` times the FP64 CPU oracle (the reference of this
+project) on the host cores on the same workload and metric, each step a
+bounded sample (a subset of the batch's sequences); under torchrun only rank 0
+runs it.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ------------------------------------------------------------------ bookkeeping
+
+def decode_kv_bytes(case) -> int:
+    """K+V bytes the method must read: sum_b min(L_b, max) * Hkv * D * 2 * elem."""
+    L = np.clip(case.seq_lens.astype(np.int64), 0, case.max_seq_len)
+    return int(L.sum()) * case.Hkv * case.D * 2 * case.kv.itemsize
+
+
+def prefill_tokens(case) -> int:
+    """Tokens the rows attend to: 4 per selected block before the row's own
+    block, plus the row's causal tail."""
+    p = np.minimum(case.q_pos.astype(np.int64), case.kv_len - 1)
+    own = p // 4
+    sel = (case.sel_idx >= 0) & (case.sel_idx < own[:, None])
+    live = case.q_pos >= 0
+    return int(4 * sel[live].sum() + (p - 4 * own + 1)[live].sum())
+
+
+def source_hash() -> str:
+    """Hash of the CUDA sources; ncu traffic figures are tied to it."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "fp8_kv_cache_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def ncu_traffic(kernel_tag: str):
+    """Per-launch DRAM bytes of a kernel from a committed ncu summary, if it
+    was taken on the current sources (else None)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel_tag}.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    if d.get("source_hash") != source_hash():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi SM clock / throttle-reason samples while timed work runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines += [ln for ln in out.splitlines() if ln.strip()]
+        self.proc = None
+
+    def summary(self):
+        rows = []
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append((float(f[1]), float(f[2]), float(f[4]), f[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        loaded = [r for r in rows if r[2] >= 50.0] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in loaded for i, v in enumerate(r[3]) if v == "Active"})
+        return {"sm_mhz": statistics.median(r[0] for r in loaded),
+                "sm_max_mhz": max(r[1] for r in loaded), "reasons": reasons,
+                "samples": len(loaded)}
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, rank, world):
+    import torch
+    import fp8_kv_cache_gb300 as P
+    from fp8_kv_cache_gb300 import build as Bld
+    from fp8_kv_cache_gb300 import workloads as W
+
+    Bld.build()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+
+    case = W.long_e4m3()
+    kvb = decode_kv_bytes(case)
+    kv = torch.from_numpy(case.kv).to(dev)
+    k, v = kv[0], kv[1]
+    q = torch.from_numpy(case.q).to(dev)
+    bt = torch.from_numpy(case.block_table).to(dev)
+    sl = torch.from_numpy(case.seq_lens).to(dev)
+    out = torch.empty_like(q)
+    ws = torch.empty(P.paged_gqa_decode_workspace_size(case.B, case.Hq, case.Hkv, case.D,
+                                                       case.max_seq_len),
+                     dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def decode(evs=None):
+        P.paged_gqa_decode(q, k, v, bt, sl, case.page_size, case.kv_scale, case.softmax_scale, out,
+                           max_seq_len=case.max_seq_len, workspace=ws, split_events=evs)
+
+    K, Wm = args.steps, args.warmup
+    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    for _ in range(Wm):
+        decode()
+        flush.zero_()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    clocks.start()
+    time.sleep(0.25)
+    starts, ends = [mk() for _ in range(K)], [mk() for _ in range(K)]
+    ks, ke = [mk() for _ in range(K)], [mk() for _ in range(K)]
+    for e in ks + ke:
+        e.record()                           # creates the events before their handles are used
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(K):
+        starts[i].record()
+        decode((ks[i], ke[i]))
+        ends[i].record()
+        flush.zero_()
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    step_ms = [starts[i].elapsed_time(ends[i]) for i in range(K)]
+    split_ms = [ks[i].elapsed_time(ke[i]) for i in range(K)]
+    total_ms = float(sum(step_ms))
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / K
+    value = world * kvb * K / (total_ms * 1e-3) / 1e9
+
+    # ---- end to end: per-step inputs from pinned host memory, result back
+    q_h = torch.from_numpy(case.q).pin_memory()
+    bt_h = torch.from_numpy(case.block_table).pin_memory()
+    sl_h = torch.from_numpy(case.seq_lens).pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = q_h.numel() * 2 + bt_h.numel() * 4 + sl_h.numel() * 4
+    d2h = out_h.numel() * 2
+    Ke = max(1, min(K, 200))
+
+    def e2e_step():
+        q.copy_(q_h, non_blocking=True)
+        bt.copy_(bt_h, non_blocking=True)
+        sl.copy_(sl_h, non_blocking=True)
+        decode()
+        out_h.copy_(out, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+        flush.zero_()
+    torch.cuda.synchronize()
+    e_ms = 0.0
+    for _ in range(Ke):
+        a, b = mk(), mk()
+        a.record()
+        e2e_step()
+        b.record()
+        flush.zero_()
+        torch.cuda.synchronize()
+        e_ms += a.elapsed_time(b)
+    e2e_value = world * kvb * Ke / (e_ms * 1e-3) / 1e9
+
+    # ---- selected-sparse prefill, 4096 rows
+    pc = W.sparse_prefill_4096()
+    pkv = torch.from_numpy(pc.kv).to(dev)
+    pk, pv = pkv[:, :, :, 0, :], pkv[:, :, :, 1, :]
+    pq = torch.from_numpy(pc.q).to(dev)
+    pbt = torch.from_numpy(pc.block_table).to(dev)
+    psel = torch.from_numpy(pc.sel_idx).to(dev)
+    ppos = torch.from_numpy(pc.q_pos).to(dev)
+    pout = torch.empty_like(pq)
+
+    def prefill():
+        P.paged_gqa_sparse_prefill(pq, pk, pv, pbt, pc.kv_len, psel, ppos, pc.page_size,
+                                   pc.softmax_scale, pc.kv_scale, pout)
+
+    Kp = max(1, min(K, 50))
+    for _ in range(max(3, Wm)):
+        prefill()
+        flush.zero_()
+    torch.cuda.synchronize()
+    p_ms = 0.0
+    for _ in range(Kp):
+        a, b = mk(), mk()
+        a.record()
+        prefill()
+        b.record()
+        flush.zero_()
+        torch.cuda.synchronize()
+        p_ms += a.elapsed_time(b)
+    clocks.stop()
+    p_ms /= Kp
+    toks = prefill_tokens(pc)
+    row_bytes = pc.D * pc.kv.itemsize
+    gathered = toks * pc.Hkv * 2 * row_bytes
+    flops = 4.0 * toks * pc.Hq * pc.D      # QK^T and PV, 2 flops per multiply-add
+
+    peak, peak_kind = measured_peaks()
+    split_avg = float(np.mean(split_ms))
+    achieved = kvb / (split_avg * 1e-3) / 1e9
+    line = {
+        "metric": "paged GQA D256 decode KV-read GB/s (FP8-E4M3 KV, GQA-6)",
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": Wm,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16",
+        "data": "synthetic (seeded PCG64; N(0,1)*2 quantised to E4M3 with a per-tensor scale)",
+        "config": {
+            "workload": "long-context E4M3 decode: B=16, Hkv=4, Hq=24, D=256, seq_lens "
+                        "U[12288,16384], page 16, 16384-page shuffled pool",
+            "kv_dtype": "e4m3", "global_batch": case.B, "seq_lens_sum": int(case.seq_lens.sum()),
+            "kv_bytes_per_step": kvb, "parallelism": f"replicas x{world}",
+            "l2": "256 MB buffer written between steps (outside the timed events); "
+                  "KV per step (470 MB) also exceeds the 129 MB L2",
+        },
+        "decode_tok_s": round(world * case.B / (ms_per_step * 1e-3), 1),
+        "roofline": {
+            "kernel": "decode_split_kernel<E4M3>",
+            "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
+            "traffic": ncu_traffic("decode_split_long_e4m3"),
+            "algorithmic_bytes_per_launch": kvb, "avg_launch_ms": round(split_avg, 5),
+        },
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": Ke,
+                "note": "per-step q, block table and seq_lens copied from pinned host memory "
+                        "and the output copied back inside the timed region; the KV cache is "
+                        "the attention's resident device state"},
+        "sparse_prefill": {
+            "workload": "4096 rows, Hq6/Hkv1/D256 FP16, interleaved K/V, 512 selected "
+                        "four-token blocks + 1..3-token tail, 32768-token cache (2048 pages)",
+            "ms": round(p_ms, 4), "rows_per_s": round(world * pc.R / (p_ms * 1e-3), 1),
+            "tokens_attended": toks,
+            "gathered_GBps": round(gathered / (p_ms * 1e-3) / 1e9, 1),
+            "tflops": round(flops / (p_ms * 1e-3) / 1e12, 2),
+            "pages_context_ms_v100": 8.84736,
+        },
+        "gpu_launches": 2 * K,
+        "clocks": clocks.summary(),
+        "wall_s_timed_decode": round(wall, 4),
+    }
+    return line
+
+
+def cpu_baseline(sample_seqs=4, threads=None):
+    """The FP64 oracle on the first ``sample_seqs`` sequences of the decode
+    workload, all heads; returns (GB/s-equivalent of KV processed, dict)."""
+    import oracle
+    from fp8_kv_cache_gb300 import workloads as W
+    case = W.long_e4m3()
+    sub = slice(0, sample_seqs)
+    threads = threads or oracle.default_threads()
+    t0 = time.perf_counter()
+    oracle.decode(case.q[sub], case.k, case.v, case.block_table[sub], case.seq_lens[sub],
+                  case.page_size, case.num_pages, case.max_seq_len, case.kv_scale,
+                  case.softmax_scale, threads=threads)
+    dt = time.perf_counter() - t0
+    L = np.clip(case.seq_lens[sub].astype(np.int64), 0, case.max_seq_len)
+    kvb = int(L.sum()) * case.Hkv * case.D * 2
+    return kvb / dt / 1e9, {"value": round(kvb / dt / 1e9, 5), "unit": "GB/s",
+                            "cores": threads, "kind": "oracle",
+                            "sample": f"decode of sequences 0..{sample_seqs - 1} of the workload "
+                                      f"(all 24 heads, {int(L.sum())} tokens), FP64 C oracle, "
+                                      f"{dt:.2f} s"}
+
+
+def run_reference(args, world):
+    """The FP64 CPU oracle timed per step on a bounded sample of the workload."""
+    import oracle
+    from fp8_kv_cache_gb300 import workloads as W
+    case = W.long_e4m3()
+    threads = oracle.default_threads()
+    per_step = 1                                # one sequence, all heads, per step
+    kvb_step = 0
+    times = []
+    for i in range(args.warmup + args.steps):
+        b = i % case.B
+        sub = slice(b, b + per_step)
+        t0 = time.perf_counter()
+        oracle.decode(case.q[sub], case.k, case.v, case.block_table[sub], case.seq_lens[sub],
+                      case.page_size, case.num_pages, case.max_seq_len, case.kv_scale,
+                      case.softmax_scale, threads=threads)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+            kvb_step += int(min(case.seq_lens[b], case.max_seq_len)) * case.Hkv * case.D * 2
+    total = sum(times)
+    value = kvb_step / total / 1e9
+    return {
+        "impl": "reference",
+        "metric": "paged GQA D256 decode KV-read GB/s (FP8-E4M3 KV, GQA-6)",
+        "value": round(value, 5), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(1e3 * total / len(times), 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded PCG64)",
+        "config": {"workload": "long-context E4M3 decode: B=16, Hkv=4, Hq=24, D=256, seq_lens "
+                               "U[12288,16384], page 16, 16384-page shuffled pool",
+                   "sample_per_step": "one sequence (all 24 heads), cycling through the batch"},
+        "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": threads,
+                         "kind": "oracle", "sample": "one sequence of the batch per step"},
+        "e2e": {"value": round(value, 5), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, world)), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        dist.init_process_group("nccl")
+    line = run_ours(args, rank, world)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            _, line["cpu_baseline"] = cpu_baseline()
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,311 @@
+// api.cu -- the extern "C" entry points declared in include/paged_gqa.h:
+// host-side validation, the split-count choice and the launches.  Nothing
+// here allocates memory or synchronises the host.
+#include <atomic>
+#include <cmath>
+
+#include "pgqa_internal.h"
+
+using namespace pgqa;
+
+namespace {
+
+constexpr double kLog2e = 1.4426950408889634;
+
+bool aligned16(const void* p)
+{
+    return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+int elem_bytes(int kv_dtype)
+{
+    return kv_dtype == PAGED_GQA_KV_E4M3 ? 1 : 2;
+}
+
+int log2_if_pow2(int x)
+{
+    if (x <= 0 || (x & (x - 1)) != 0)
+        return -1;
+    int s = 0;
+    while ((1 << s) < x)
+        ++s;
+    return s;
+}
+
+// Common checks of the KV pools and layout.
+int check_kv(const void* k, const void* v, const paged_gqa_kv_layout& L, int kv_dtype)
+{
+    if (kv_dtype != PAGED_GQA_KV_FP16 && kv_dtype != PAGED_GQA_KV_E4M3)
+        return PAGED_GQA_ERR_UNSUPPORTED;
+    if (k == nullptr || v == nullptr)
+        return PAGED_GQA_ERR_NULL_POINTER;
+    if (!aligned16(k) || !aligned16(v))
+        return PAGED_GQA_ERR_ALIGNMENT;
+    if (L.page_stride < 0 || L.token_stride < 0 || L.head_stride < 0)
+        return PAGED_GQA_ERR_SHAPE;
+    const int64_t e = elem_bytes(kv_dtype);
+    if ((L.page_stride * e) % 16 || (L.token_stride * e) % 16 || (L.head_stride * e) % 16)
+        return PAGED_GQA_ERR_ALIGNMENT;
+    return PAGED_GQA_OK;
+}
+
+KVGeom make_geom(const void* k, const void* v, const paged_gqa_kv_layout& L, int kv_dtype,
+                 int page_size, int num_pages)
+{
+    const int64_t e = elem_bytes(kv_dtype);
+    KVGeom g;
+    g.k = static_cast<const unsigned char*>(k);
+    g.v = static_cast<const unsigned char*>(v);
+    g.page_b = L.page_stride * e;
+    g.token_b = L.token_stride * e;
+    g.head_b = L.head_stride * e;
+    g.page_size = page_size;
+    g.page_shift = log2_if_pow2(page_size);
+    g.num_pages = num_pages;
+    return g;
+}
+
+// Per-device cache of the SM count and of the split kernel's CTAs per SM.
+struct DeviceInfo {
+    int sms;
+    int ctas_fp16;
+    int ctas_e4m3;
+};
+
+int device_info(DeviceInfo& out)
+{
+    static std::atomic<int> sms[kMaxDevices], c16[kMaxDevices], c8[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return PAGED_GQA_ERR_CUDA;
+    if (dev < kMaxDevices && sms[dev].load(std::memory_order_acquire) > 0) {
+        out.sms = sms[dev].load(std::memory_order_acquire);
+        out.ctas_fp16 = c16[dev].load(std::memory_order_relaxed);
+        out.ctas_e4m3 = c8[dev].load(std::memory_order_relaxed);
+        return PAGED_GQA_OK;
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        return PAGED_GQA_ERR_CUDA;
+    out.sms = n;
+    out.ctas_fp16 = split_ctas_per_sm(false);
+    out.ctas_e4m3 = split_ctas_per_sm(true);
+    if (dev < kMaxDevices) {
+        c16[dev].store(out.ctas_fp16, std::memory_order_relaxed);
+        c8[dev].store(out.ctas_e4m3, std::memory_order_relaxed);
+        sms[dev].store(n, std::memory_order_release);
+    }
+    return PAGED_GQA_OK;
+}
+
+int check_decode_shape(int B, int Hq, int Hkv, int D, int max_seq_len)
+{
+    if (B < 0 || Hq < 1 || Hkv < 1 || max_seq_len < 0)
+        return PAGED_GQA_ERR_SHAPE;
+    if (Hq % Hkv != 0)
+        return PAGED_GQA_ERR_SHAPE;
+    if (D != kD || Hq / Hkv > kGMax)
+        return PAGED_GQA_ERR_UNSUPPORTED;
+    return PAGED_GQA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int paged_gqa_version(void)
+{
+    return PAGED_GQA_VERSION;
+}
+
+const char* paged_gqa_status_string(int status)
+{
+    switch (status) {
+    case PAGED_GQA_OK: return "ok";
+    case PAGED_GQA_ERR_NULL_POINTER: return "a required pointer is NULL";
+    case PAGED_GQA_ERR_ALIGNMENT: return "a pointer or stride is not 16-byte aligned";
+    case PAGED_GQA_ERR_SHAPE: return "inconsistent or out-of-range sizes";
+    case PAGED_GQA_ERR_UNSUPPORTED: return "unsupported head dim, group size or KV dtype";
+    case PAGED_GQA_ERR_WORKSPACE: return "workspace too small or misaligned";
+    case PAGED_GQA_ERR_CUDA: return "a CUDA runtime call or launch failed";
+    default: return "unknown status";
+    }
+}
+
+size_t paged_gqa_decode_workspace_size(int B, int Hq, int Hkv, int D, int max_seq_len)
+{
+    if (check_decode_shape(B, Hq, Hkv, D, max_seq_len) != PAGED_GQA_OK)
+        return 0;
+    if (B > kMaxSplitBatch)
+        return 0;   // such batches take the unsplit route
+    DeviceInfo di;
+    if (device_info(di) != PAGED_GQA_OK)
+        return 0;
+    const int per = di.ctas_fp16 > di.ctas_e4m3 ? di.ctas_fp16 : di.ctas_e4m3;
+    return workspace_bytes(B, Hkv, di.sms * per);
+}
+
+size_t paged_gqa_decode_workspace_size_splits(int B, int Hq, int Hkv, int D, int splits)
+{
+    if (check_decode_shape(B, Hq, Hkv, D, 0) != PAGED_GQA_OK || splits < 1 || B > kMaxSplitBatch)
+        return 0;
+    return workspace_bytes(B, Hkv, splits);
+}
+
+int paged_gqa_decode(const void* q, const void* k_cache, const void* v_cache,
+                     paged_gqa_kv_layout kv_layout, int kv_dtype, const int32_t* block_table,
+                     int64_t bt_row_stride, const int32_t* seq_lens, int B, int Hq, int Hkv, int D,
+                     int page_size, int num_pages, int max_seq_len, float kv_scale,
+                     float softmax_scale, void* out, const paged_gqa_workspace* ws, void* stream)
+{
+    int st = check_decode_shape(B, Hq, Hkv, D, max_seq_len);
+    if (st != PAGED_GQA_OK)
+        return st;
+    if (page_size < 1 || num_pages < 1 || bt_row_stride < 0)
+        return PAGED_GQA_ERR_SHAPE;
+    if (B > 1 && bt_row_stride < (int64_t)((max_seq_len + page_size - 1) / page_size))
+        return PAGED_GQA_ERR_SHAPE;
+    if ((st = check_kv(k_cache, v_cache, kv_layout, kv_dtype)) != PAGED_GQA_OK)
+        return st;
+    if (q == nullptr || block_table == nullptr || seq_lens == nullptr || out == nullptr)
+        return PAGED_GQA_ERR_NULL_POINTER;
+    if (!aligned16(q) || !aligned16(out))
+        return PAGED_GQA_ERR_ALIGNMENT;
+    if (B == 0)
+        return PAGED_GQA_OK;
+
+    const bool e4m3 = kv_dtype == PAGED_GQA_KV_E4M3;
+    DecodeArgs a{};
+    a.q = static_cast<const __half*>(q);
+    a.kv = make_geom(k_cache, v_cache, kv_layout, kv_dtype, page_size, num_pages);
+    a.bt = block_table;
+    a.bt_stride = bt_row_stride;
+    a.seq_lens = seq_lens;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.G = Hq / Hkv;
+    a.max_seq_len = max_seq_len;
+    a.scale_log2 = (float)((double)softmax_scale * (e4m3 ? (double)kv_scale : 1.0) * kLog2e);
+    a.v_scale = e4m3 ? kv_scale : 1.f;
+    a.out = static_cast<__half*>(out);
+    a.err = ws ? ws->err_flag : nullptr;
+    a.C = 0;
+
+    const bool split = ws != nullptr && ws->ptr != nullptr && B <= kMaxSplitBatch;
+    if (split) {
+        if ((reinterpret_cast<uintptr_t>(ws->ptr) & 255u) != 0)
+            return PAGED_GQA_ERR_WORKSPACE;
+        DeviceInfo di;
+        if (device_info(di) != PAGED_GQA_OK)
+            return PAGED_GQA_ERR_CUDA;
+        int C = ws->force_splits > 0 ? ws->force_splits
+                                     : di.sms * (e4m3 ? di.ctas_e4m3 : di.ctas_fp16);
+        if (workspace_bytes(B, Hkv, C) > ws->bytes)
+            return PAGED_GQA_ERR_WORKSPACE;
+        size_t head = kHeaderBytes + (size_t)(B + 1) * sizeof(int64_t);
+        head = (head + 255) & ~(size_t)255;
+        a.hdr = static_cast<int64_t*>(ws->ptr);
+        a.slots = reinterpret_cast<float*>(static_cast<unsigned char*>(ws->ptr) + head);
+        a.C = C;
+        a.min_tiles = ws->force_splits > 0 ? 0 : 8;
+    }
+    void* ev0 = ws ? ws->split_events[0] : nullptr;
+    void* ev1 = ws ? ws->split_events[1] : nullptr;
+    const cudaError_t e = launch_decode(a, e4m3, static_cast<cudaStream_t>(stream), ev0, ev1);
+    return e == cudaSuccess ? PAGED_GQA_OK : PAGED_GQA_ERR_CUDA;
+}
+
+int paged_gqa_sparse_prefill(const void* q, const void* k_cache, const void* v_cache,
+                             paged_gqa_kv_layout kv_layout, int kv_dtype,
+                             const int32_t* block_table, int num_pages, int kv_len,
+                             const int32_t* sel_idx, int n_sel, const int32_t* q_pos, int R,
+                             int Hq, int Hkv, int D, int page_size, float kv_scale,
+                             float softmax_scale, void* out, int* err_flag, void* stream)
+{
+    if (R < 0 || n_sel < 0 || Hq < 1 || Hkv < 1 || kv_len < 0 || Hq % Hkv != 0)
+        return PAGED_GQA_ERR_SHAPE;
+    if (D != kD || Hq / Hkv > kGMax)
+        return PAGED_GQA_ERR_UNSUPPORTED;
+    if (page_size < 4 || page_size % 4 != 0 || num_pages < 1 || Hkv > 65535)
+        return PAGED_GQA_ERR_SHAPE;
+    if (n_sel > (1 << 28))
+        return PAGED_GQA_ERR_SHAPE;
+    int st = check_kv(k_cache, v_cache, kv_layout, kv_dtype);
+    if (st != PAGED_GQA_OK)
+        return st;
+    if (q == nullptr || block_table == nullptr || q_pos == nullptr || out == nullptr ||
+        (n_sel > 0 && sel_idx == nullptr))
+        return PAGED_GQA_ERR_NULL_POINTER;
+    if (!aligned16(q) || !aligned16(out))
+        return PAGED_GQA_ERR_ALIGNMENT;
+    if (R == 0)
+        return PAGED_GQA_OK;
+    const bool e4m3 = kv_dtype == PAGED_GQA_KV_E4M3;
+    PrefillArgs a{};
+    a.q = static_cast<const __half*>(q);
+    a.kv = make_geom(k_cache, v_cache, kv_layout, kv_dtype, page_size, num_pages);
+    a.bt = block_table;
+    a.kv_len = kv_len;
+    a.sel = sel_idx;
+    a.n_sel = n_sel;
+    a.q_pos = q_pos;
+    a.R = R;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.G = Hq / Hkv;
+    a.scale_log2 = (float)((double)softmax_scale * (e4m3 ? (double)kv_scale : 1.0) * kLog2e);
+    a.v_scale = e4m3 ? kv_scale : 1.f;
+    a.out = static_cast<__half*>(out);
+    a.err = err_flag;
+    const cudaError_t e = launch_prefill(a, e4m3, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PAGED_GQA_OK : PAGED_GQA_ERR_CUDA;
+}
+
+int paged_gqa_gather_dequant(const void* cache, paged_gqa_kv_layout kv_layout, int kv_dtype,
+                             const int32_t* block_table, int64_t bt_row_stride,
+                             const int32_t* seq_lens, int B, int T, int Hkv, int D, int page_size,
+                             int num_pages, int max_seq_len, float kv_scale, float* out,
+                             void* stream)
+{
+    if (B < 0 || T < 0 || Hkv < 1 || page_size < 1 || num_pages < 1 || max_seq_len < 0 ||
+        bt_row_stride < 0 || B > 65535 || Hkv > 65535)
+        return PAGED_GQA_ERR_SHAPE;
+    if (D != kD)
+        return PAGED_GQA_ERR_UNSUPPORTED;
+    int st = check_kv(cache, cache, kv_layout, kv_dtype);
+    if (st != PAGED_GQA_OK)
+        return st;
+    if (block_table == nullptr || seq_lens == nullptr || out == nullptr)
+        return PAGED_GQA_ERR_NULL_POINTER;
+    if (!aligned16(out))
+        return PAGED_GQA_ERR_ALIGNMENT;
+    if (B == 0 || T == 0)
+        return PAGED_GQA_OK;
+    const KVGeom g = make_geom(cache, cache, kv_layout, kv_dtype, page_size, num_pages);
+    const cudaError_t e = launch_gather(g, kv_dtype == PAGED_GQA_KV_E4M3, block_table,
+                                       bt_row_stride, seq_lens, B, T, Hkv, max_seq_len, kv_scale,
+                                       out, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PAGED_GQA_OK : PAGED_GQA_ERR_CUDA;
+}
+
+int paged_gqa_sparse_prefill_tokens(const int32_t* block_table, int num_pages, int kv_len,
+                                    const int32_t* sel_idx, int n_sel, const int32_t* q_pos,
+                                    int R, int page_size, int32_t* out, void* stream)
+{
+    if (R < 0 || n_sel < 0 || kv_len < 0 || num_pages < 1 || page_size < 4 ||
+        page_size % 4 != 0 || n_sel > (1 << 28))
+        return PAGED_GQA_ERR_SHAPE;
+    if (block_table == nullptr || q_pos == nullptr || out == nullptr ||
+        (n_sel > 0 && sel_idx == nullptr))
+        return PAGED_GQA_ERR_NULL_POINTER;
+    if (R == 0)
+        return PAGED_GQA_OK;
+    paged_gqa_kv_layout L{0, 0, 0};
+    const KVGeom g = make_geom(nullptr, nullptr, L, PAGED_GQA_KV_FP16, page_size, num_pages);
+    const cudaError_t e = launch_prefill_tokens(g, block_table, kv_len, sel_idx, n_sel, q_pos, R,
+                                                out, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PAGED_GQA_OK : PAGED_GQA_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,313 @@
+// decode.cu -- batched paged GQA decode: split kernel + LSE-merge kernel.
+//
+// Operation: "[Kernel][SM70] Scale NVFP4 E4M3 decode batches" (1Cat-vLLM
+// #282), Purpose: FP8-E4M3 (or FP16) KV, GQA-6, head dim 256 paged decode for
+// batches of 1..16 including long contexts.
+//
+// Work decomposition (ours, not the page's V100 routing): every (sequence b,
+// KV head j) is a segment of ceil(L_b / 16) tiles; the segments are laid end
+// to end and the resulting tile line is cut into C_eff equal ranges, one per
+// CTA, so every CTA streams the same number of KV bytes whatever the mix of
+// sequence lengths.  The cut is computed on the device from seq_lens, so one
+// launch shape serves every step of a captured CUDA graph.  A CTA that covers
+// a whole segment writes the final FP16 rows; otherwise it writes an
+// unnormalised partial (m, l, O) to slot (cta + segment) of the caller's
+// workspace, and the merge kernel combines the pieces in a fixed order
+// (no floating-point atomics, so results are reproducible run to run).
+#include <atomic>
+
+#include "pgqa_internal.h"
+
+namespace pgqa {
+
+namespace {
+
+__device__ __forceinline__ int clamp_len(int L, int max_len)
+{
+    return L < 0 ? 0 : (L > max_len ? max_len : L);
+}
+
+// Largest b in [0, B) with Hkv * P[b] <= x (P non-decreasing, x < Hkv * P[B]).
+__device__ __forceinline__ int find_seq(const int64_t* P, int B, int Hkv, int64_t x)
+{
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if ((int64_t)Hkv * P[mid] <= x)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    return lo;
+}
+
+// The tiles [ta, te) of segment (b, j) processed by this CTA's warps (as
+// half-tiles of 8 tokens, round-robin), then merged into out_rows (final) or
+// slot (partial).
+template <bool kE4M3>
+__device__ void run_piece(const DecodeArgs& a, MergeSmem& sm, int b, int j, int L, int ta,
+                          int te, __half* out_rows, float* slot, int& flags)
+{
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int g = lane >> 2, q = lane & 3;
+    using Core = WarpCore<kE4M3>;
+    uint2* qs = q_stage(sm, w);
+    Core::stage_q(qs, a.q + ((size_t)b * a.Hq + (size_t)j * a.G) * kD, a.G, lane);
+    Core wc;
+    wc.reset();
+    const int32_t* bt_row = a.bt + (int64_t)b * a.bt_stride;
+    auto offsets = [&](int h, int64_t& ok, int64_t& o0, int64_t& o1) {
+        int64_t off = -1;
+        if (lane < kHalf) {
+            const int t = h * kHalf + lane;
+            if (t < L)
+                off = token_row_offset(a.kv, bt_row, t, j, flags);
+        }
+        ok = __shfl_sync(0xffffffffu, off, g);
+        o0 = __shfl_sync(0xffffffffu, off, 2 * q);
+        o1 = __shfl_sync(0xffffffffu, off, 2 * q + 1);
+    };
+    run_halves<kE4M3, kRing<kE4M3>()>(wc, qs, a.kv.k, a.kv.v, 2 * ta + w, 2 * te, kWarps,
+                                      g < a.G, a.scale_log2, lane, offsets);
+    cta_merge<kE4M3>(sm, wc, a.G, a.v_scale, out_rows, slot);
+}
+
+__device__ void zero_rows(__half* rows, int G)
+{
+    for (int i = threadIdx.x; i < G * kD; i += blockDim.x)
+        rows[i] = __float2half_rn(0.f);
+}
+
+}  // namespace
+
+template <bool kE4M3>
+__global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(DecodeArgs a)
+{
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    MergeSmem& sm = *reinterpret_cast<MergeSmem*>(smem_raw);
+    int flags = 0;
+
+    if (a.C == 0) {
+        // ---- unsplit route: CTA = one whole segment
+        const int k = blockIdx.x;
+        const int b = k / a.Hkv, j = k - b * a.Hkv;
+        const int raw = __ldg(a.seq_lens + b);
+        const int L = clamp_len(raw, a.max_seq_len);
+        __half* out_rows = a.out + ((size_t)b * a.Hq + (size_t)j * a.G) * kD;
+        if (threadIdx.x == 0) {
+            if (raw > a.max_seq_len) flags |= PAGED_GQA_FLAG_SEQ_CLAMPED;
+            if (raw <= 0) flags |= PAGED_GQA_FLAG_EMPTY_ROW;
+        }
+        if (L == 0) {
+            zero_rows(out_rows, a.G);
+        } else {
+            run_piece<kE4M3>(a, sm, b, j, L, 0, (L + kTile - 1) / kTile, out_rows, nullptr, flags);
+        }
+        raise_flag(a.err, flags);
+        return;
+    }
+
+    // ---- split route: exclusive prefix P[b] of per-sequence tile counts
+    int64_t* P = reinterpret_cast<int64_t*>(smem_raw + sizeof(MergeSmem));
+    int64_t* wtot = P + (a.B + 1);
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int per = (a.B + kThreads - 1) / kThreads;
+    const int b0 = min(a.B, tid * per), b1 = min(a.B, b0 + per);
+    int64_t local = 0;
+    for (int b = b0; b < b1; ++b) {
+        const int raw = __ldg(a.seq_lens + b);
+        if (blockIdx.x == 0) {
+            if (raw > a.max_seq_len) flags |= PAGED_GQA_FLAG_SEQ_CLAMPED;
+            if (raw <= 0) flags |= PAGED_GQA_FLAG_EMPTY_ROW;
+        }
+        local += (clamp_len(raw, a.max_seq_len) + kTile - 1) / kTile;
+    }
+    int64_t incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int64_t t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    if (lane == 31) wtot[w] = incl;
+    __syncthreads();
+    int64_t base = 0, total = 0;
+    for (int i = 0; i < kWarps; ++i) {
+        if (i < w) base += wtot[i];
+        total += wtot[i];
+    }
+    int64_t run = base + incl - local;
+    for (int b = b0; b < b1; ++b) {
+        P[b] = run;
+        run += (clamp_len(__ldg(a.seq_lens + b), a.max_seq_len) + kTile - 1) / kTile;
+    }
+    if (tid == 0) P[a.B] = total;
+    __syncthreads();
+
+    const int64_t T = (int64_t)a.Hkv * total;
+    int64_t C = a.C;
+    if (a.min_tiles > 0) {
+        const int64_t want = (T + a.min_tiles - 1) / a.min_tiles;
+        C = max((int64_t)1, min(C, want));
+    }
+    if (blockIdx.x == 0) {
+        for (int i = tid; i <= a.B; i += kThreads)
+            a.hdr[2 + i] = P[i];
+        if (tid == 0) {
+            a.hdr[0] = T;
+            a.hdr[1] = C;
+        }
+    }
+    const int64_t c = blockIdx.x;
+    if (c >= C || T == 0) {
+        raise_flag(a.err, flags);
+        return;
+    }
+    const int64_t x0 = c * T / C, x1 = (c + 1) * T / C;
+    if (x0 >= x1) {
+        raise_flag(a.err, flags);
+        return;
+    }
+    int b = find_seq(P, a.B, a.Hkv, x0);
+    int64_t nb = P[b + 1] - P[b];
+    int j = (int)((x0 - (int64_t)a.Hkv * P[b]) / nb);
+    for (;;) {
+        const int64_t s0 = (int64_t)a.Hkv * P[b] + (int64_t)j * nb;
+        const int64_t s1 = s0 + nb;
+        if (s0 >= x1)
+            break;
+        const int ta = (int)(max(x0, s0) - s0), te = (int)(min(x1, s1) - s0);
+        const int L = clamp_len(__ldg(a.seq_lens + b), a.max_seq_len);
+        const int64_t k = (int64_t)b * a.Hkv + j;
+        const bool whole = x0 <= s0 && x1 >= s1;
+        __half* out_rows = whole ? a.out + ((size_t)b * a.Hq + (size_t)j * a.G) * kD : nullptr;
+        float* slot = whole ? nullptr : a.slots + (size_t)(c + k) * kSlotFloats;
+        run_piece<kE4M3>(a, sm, b, j, L, ta, te, out_rows, slot, flags);
+        // next non-empty segment
+        if (++j == a.Hkv) {
+            j = 0;
+            do {
+                ++b;
+            } while (b < a.B && P[b + 1] == P[b]);
+            if (b >= a.B)
+                break;
+            nb = P[b + 1] - P[b];
+        }
+    }
+    raise_flag(a.err, flags);
+}
+
+// One CTA per segment (grid Hkv x B): zero rows for empty segments, nothing
+// for segments one split CTA covered, else the fixed-order LSE merge
+//   M = max m_i,  O = sum_i 2^(m_i - M) O_i / sum_i 2^(m_i - M) l_i.
+__global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeArgs a)
+{
+    const int j = blockIdx.x, b = blockIdx.y;
+    const int64_t T = a.hdr[0], C = a.hdr[1];
+    const int64_t* P = a.hdr + 2;
+    const int64_t nb = P[b + 1] - P[b];
+    __half* out_rows = a.out + ((size_t)b * a.Hq + (size_t)j * a.G) * kD;
+    if (nb == 0) {
+        zero_rows(out_rows, a.G);
+        return;
+    }
+    const int64_t s0 = (int64_t)a.Hkv * P[b] + (int64_t)j * nb;
+    const int64_t s1 = s0 + nb;
+    const int64_t c_first = ((s0 + 1) * C + T - 1) / T - 1;
+    const int64_t c_last = (s1 * C + T - 1) / T - 1;
+    if (c_first == c_last)
+        return;
+    const int64_t k = (int64_t)b * a.Hkv + j;
+    const int d = threadIdx.x;
+    // CTAs with an empty tile range (possible when C > T) wrote no slot.
+    auto empty = [&](int64_t c) { return c * T / C == (c + 1) * T / C; };
+    for (int h = 0; h < a.G; ++h) {
+        float M = -INFINITY;
+        for (int64_t c = c_first; c <= c_last; ++c)
+            if (!empty(c))
+                M = fmaxf(M, a.slots[(size_t)(c + k) * kSlotFloats + h]);
+        float num = 0.f, den = 0.f;
+        if (M != -INFINITY) {
+            for (int64_t c = c_first; c <= c_last; ++c) {
+                if (empty(c))
+                    continue;
+                const float* sl = a.slots + (size_t)(c + k) * kSlotFloats;
+                const float e = ex2(sl[h] - M);
+                den += e * sl[kGMax + h];
+                num += e * sl[2 * kGMax + h * kD + d];
+            }
+        }
+        out_rows[(size_t)h * kD + d] = __float2half_rn(den > 0.f ? num / den * a.v_scale : 0.f);
+    }
+}
+
+size_t decode_split_smem(int B)
+{
+    return sizeof(MergeSmem) + (size_t)(B + 1) * sizeof(int64_t) + kWarps * sizeof(int64_t);
+}
+
+size_t workspace_bytes(int B, int Hkv, int C)
+{
+    size_t head = kHeaderBytes + (size_t)(B + 1) * sizeof(int64_t);
+    head = (head + 255) & ~(size_t)255;
+    return head + ((size_t)C + (size_t)B * Hkv) * kSlotFloats * sizeof(float);
+}
+
+// The dynamic shared-memory opt-in is a per-device function attribute; it is
+// set once per device and kernel instantiation.
+template <bool kE4M3>
+static cudaError_t set_smem_attr()
+{
+    static std::atomic<int> done[kMaxDevices];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < kMaxDevices && done[dev].load(std::memory_order_acquire))
+        return cudaSuccess;
+    e = cudaFuncSetAttribute(decode_split_kernel<kE4M3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)decode_split_smem(kMaxSplitBatch));
+    if (e == cudaSuccess && dev < kMaxDevices)
+        done[dev].store(1, std::memory_order_release);
+    return e;
+}
+
+int split_ctas_per_sm(bool e4m3)
+{
+    int n = 0;
+    const size_t smem = decode_split_smem(64);
+    cudaError_t e = e4m3 ? set_smem_attr<true>() : set_smem_attr<false>();
+    if (e != cudaSuccess)
+        return 1;
+    if (e4m3)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_split_kernel<true>, kThreads, smem);
+    else
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_split_kernel<false>, kThreads, smem);
+    return (e == cudaSuccess && n > 0) ? n : 1;
+}
+
+cudaError_t launch_decode(const DecodeArgs& a, bool e4m3, cudaStream_t s, void* ev0, void* ev1)
+{
+    cudaError_t e = e4m3 ? set_smem_attr<true>() : set_smem_attr<false>();
+    if (e != cudaSuccess)
+        return e;
+    const int grid = a.C > 0 ? a.C : a.B * a.Hkv;
+    const size_t smem = a.C > 0 ? decode_split_smem(a.B) : sizeof(MergeSmem);
+    if (ev0 && ev1 && (e = cudaEventRecord((cudaEvent_t)ev0, s)) != cudaSuccess)
+        return e;
+    if (e4m3)
+        decode_split_kernel<true><<<grid, kThreads, smem, s>>>(a);
+    else
+        decode_split_kernel<false><<<grid, kThreads, smem, s>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess)
+        return e;
+    if (ev0 && ev1 && (e = cudaEventRecord((cudaEvent_t)ev1, s)) != cudaSuccess)
+        return e;
+    if (a.C > 0) {
+        decode_merge_kernel<<<dim3(a.Hkv, a.B), kMergeThreads, 0, s>>>(a);
+        if ((e = cudaGetLastError()) != cudaSuccess)
+            return e;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace pgqa

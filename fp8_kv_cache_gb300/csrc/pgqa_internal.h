@@ -1,0 +1,62 @@
+// pgqa_internal.h -- argument blocks and launch wrappers shared between the
+// host entry points (api.cu) and the kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pgqa_device.cuh"
+
+namespace pgqa {
+
+constexpr int kMaxSplitBatch = 4096;   // split route keeps a (B+1) prefix in shared memory
+constexpr int kMergeThreads = 256;
+constexpr int kHeaderBytes = 64;       // workspace header: T, C_eff
+constexpr int kMaxDevices = 64;        // per-device caches
+
+struct DecodeArgs {
+    const __half* q;
+    KVGeom kv;
+    const int32_t* bt;
+    int64_t bt_stride;
+    const int32_t* seq_lens;
+    int B, Hq, Hkv, G, max_seq_len;
+    float scale_log2;    // softmax_scale * kv_scale(K) * log2(e)
+    float v_scale;       // kv_scale for E4M3 V, 1 for FP16
+    __half* out;
+    // split route only
+    int64_t* hdr;        // [0] = T (tiles), [1] = C_eff, then prefix[B + 1]
+    float* slots;        // (C + B * Hkv) partial slots
+    int C;               // CTAs launched on the split route; 0 = unsplit route
+    int min_tiles;       // minimum tiles per CTA when choosing C_eff
+    int* err;
+};
+
+struct PrefillArgs {
+    const __half* q;
+    KVGeom kv;
+    const int32_t* bt;
+    int kv_len;
+    const int32_t* sel;
+    int n_sel;
+    const int32_t* q_pos;
+    int R, Hq, Hkv, G;
+    float scale_log2, v_scale;
+    __half* out;
+    int* err;
+};
+
+size_t decode_split_smem(int B);
+size_t workspace_bytes(int B, int Hkv, int C);
+int split_ctas_per_sm(bool e4m3);
+
+cudaError_t launch_decode(const DecodeArgs& a, bool e4m3, cudaStream_t s, void* ev0, void* ev1);
+cudaError_t launch_prefill(const PrefillArgs& a, bool e4m3, cudaStream_t s);
+cudaError_t launch_gather(const KVGeom& g, bool e4m3, const int32_t* bt, int64_t bt_stride,
+                          const int32_t* seq_lens, int B, int T, int Hkv, int max_seq_len,
+                          float kv_scale, float* out, cudaStream_t s);
+cudaError_t launch_prefill_tokens(const KVGeom& g, const int32_t* bt, int kv_len,
+                                  const int32_t* sel, int n_sel, const int32_t* q_pos, int R,
+                                  int32_t* out, cudaStream_t s);
+
+}  // namespace pgqa

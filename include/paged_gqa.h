@@ -1,0 +1,215 @@
+/*
+ * paged_gqa.h -- C ABI of the GB300 (sm_103a) paged grouped-query attention
+ * library: batched decode and selected-sparse prefill over a block-table KV
+ * cache holding FP16 or FP8-E4M3 keys and values.
+ *
+ * The operations follow two 1Cat-vLLM pull requests:
+ *   - "[Kernel][SM70] Scale NVFP4 E4M3 decode batches" (#282), Purpose:
+ *     FP8-E4M3, GQA-6, head dim 256 paged decode for batches of 1..16, with
+ *     wide KV loads, a packed E4M3 converter and long-context routes;
+ *   - "[Kernel][SM70] Accelerate Qwen3.8 QSA paged prefill" (#378), Changes:
+ *     selected-sparse prefill (Hq6/Hkv1/D256) where each query row attends to
+ *     its selected four-token blocks, read in place from the page-16 cache,
+ *     with its own causal partial block last; contiguous or interleaved K/V
+ *     strides; block tables in physical-page units; stale positions clamped
+ *     and invalid requests inert.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  * Pointers named as device data point to memory on the current CUDA
+ *    device, owned by the caller.  The library never allocates device or host
+ *    memory, never frees caller memory and holds no state between calls, so
+ *    concurrent calls from several host threads are safe.
+ *  * Every call is asynchronous on `stream` (a cudaStream_t; NULL means the
+ *    legacy default stream) and never synchronises the host, so calls can be
+ *    captured into CUDA graphs.
+ *  * Return value: PAGED_GQA_OK (0) or a negative paged_gqa_status.  Argument
+ *    errors are detected on the host before anything is launched.  A launch
+ *    failure returns PAGED_GQA_ERR_CUDA.
+ *  * Invalid data found on the device is inert rather than fatal (see the
+ *    PAGED_GQA_FLAG_* bits): it never faults, never traps, and is reported
+ *    by atomically ORing a bit into the optional device int `err_flag`.
+ *  * FP16 means IEEE binary16; E4M3 means OCP FP8 E4M3FN (bias 7, no
+ *    infinities, codes 0x7F/0xFF are NaN, largest finite 448).  An E4M3 KV
+ *    value is code_value * kv_scale; FP16 KV ignores kv_scale.
+ *  * KV layout: element d of the row of (page, slot, kv_head) lives at
+ *        cache + page*page_stride + slot*token_stride + kv_head*head_stride + d
+ *    (strides in elements of the KV type).  K and V share one layout, which
+ *    covers separate contiguous pools and one interleaved buffer.
+ *  * Logical token t of a sequence lives on page block_table_row[t / page_size]
+ *    at slot t % page_size.  Block-table entries are physical page ids into the
+ *    pool; ids outside [0, num_pages) are skipped.
+ *  * Query head h reads KV head h / (Hq / Hkv) (consecutive groups).
+ *  * Only head dim D = 256 and groups Hq / Hkv <= 8 are built.
+ */
+#ifndef PAGED_GQA_H
+#define PAGED_GQA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PAGED_GQA_VERSION 1
+
+/* Host-side status codes. */
+typedef enum {
+    PAGED_GQA_OK = 0,
+    PAGED_GQA_ERR_NULL_POINTER = -1,  /* a required pointer is NULL              */
+    PAGED_GQA_ERR_ALIGNMENT = -2,     /* a pointer or stride is not 16-byte aligned */
+    PAGED_GQA_ERR_SHAPE = -3,         /* inconsistent or out-of-range sizes      */
+    PAGED_GQA_ERR_UNSUPPORTED = -4,   /* D != 256, group > 8, unknown dtype ...  */
+    PAGED_GQA_ERR_WORKSPACE = -5,     /* workspace too small or misaligned        */
+    PAGED_GQA_ERR_CUDA = -6           /* a CUDA runtime call or launch failed     */
+} paged_gqa_status;
+
+/* Bits ORed into *err_flag by the kernels when they meet invalid data. */
+#define PAGED_GQA_FLAG_BAD_PAGE     1  /* block-table entry outside [0, num_pages): its tokens skipped */
+#define PAGED_GQA_FLAG_SEQ_CLAMPED  2  /* seq_len > max_seq_len: clamped to max_seq_len             */
+#define PAGED_GQA_FLAG_EMPTY_ROW    4  /* seq_len <= 0 or q_pos < 0: that output row is zero         */
+#define PAGED_GQA_FLAG_QPOS_CLAMPED 8  /* q_pos >= kv_len: clamped to kv_len - 1                     */
+#define PAGED_GQA_FLAG_BAD_SEL     16  /* selected block at or after the row's own block: skipped   */
+
+typedef enum {
+    PAGED_GQA_KV_FP16 = 0,            /* binary16 K/V                            */
+    PAGED_GQA_KV_E4M3 = 1             /* uint8 E4M3FN codes, times kv_scale      */
+} paged_gqa_kv_dtype;
+
+/* Strides of the K/V pools in elements of the KV type; the head-dim stride is
+ * 1.  Each stride times the element size must be a multiple of 16 bytes. */
+typedef struct {
+    int64_t page_stride;
+    int64_t token_stride;
+    int64_t head_stride;
+} paged_gqa_kv_layout;
+
+/* Caller-owned scratch for split-KV decode.
+ *  ptr/bytes     device buffer of at least paged_gqa_decode_workspace_size()
+ *                bytes, 256-byte aligned.  ptr == NULL selects the unsplit
+ *                route (one CTA per (sequence, KV head), no merge kernel).
+ *  force_splits  0 = automatic; > 0 forces that many split CTAs (tests use it
+ *                to check that the result does not depend on the split).
+ *  err_flag      optional device int receiving PAGED_GQA_FLAG_* bits.
+ *  split_events  optional pair of cudaEvent_t; when both are non-NULL the
+ *                library records [0] before and [1] after the split kernel on
+ *                `stream` (for timing that kernel alone). */
+typedef struct {
+    void* ptr;
+    size_t bytes;
+    int force_splits;
+    int* err_flag;
+    void* split_events[2];
+} paged_gqa_workspace;
+
+/*
+ * Bytes of workspace paged_gqa_decode needs for this shape on the current
+ * CUDA device (the split count depends on its SM count).  Returns 0 for
+ * invalid shapes.  Pure host function: launches nothing.
+ */
+size_t paged_gqa_decode_workspace_size(int B, int Hq, int Hkv, int D, int max_seq_len);
+
+/*
+ * Bytes of workspace needed when paged_gqa_workspace.force_splits = splits
+ * (splits > 0).  Returns 0 for invalid shapes.  Pure host function.
+ */
+size_t paged_gqa_decode_workspace_size_splits(int B, int Hq, int Hkv, int D, int splits);
+
+/*
+ * Batched paged decode ("[Kernel][SM70] Scale NVFP4 E4M3 decode batches",
+ * Purpose).  For every sequence b and query head h, with L = min(seq_lens[b],
+ * max_seq_len) and j = h / (Hq / Hkv):
+ *     out[b, h, :] = sum_{t < L} softmax_t(softmax_scale * <q[b,h,:], K_t>) V_t
+ * over the tokens t whose page is valid, K_t and V_t being rows of KV head j.
+ *
+ *  q            device, binary16 [B, Hq, D] contiguous, 16-byte aligned.
+ *  k_cache,     device, K and V pools in `kv_layout`, of kv_dtype, 16-byte
+ *  v_cache      aligned; num_pages pages of page_size tokens.
+ *  block_table  device int32, row b at block_table + b * bt_row_stride, with at
+ *               least ceil(max_seq_len / page_size) entries per row.
+ *  seq_lens     device int32 [B].
+ *  max_seq_len  host upper bound of seq_lens used to size the split; longer
+ *               sequences are clamped (PAGED_GQA_FLAG_SEQ_CLAMPED).
+ *  out          device, binary16 [B, Hq, D] contiguous, 16-byte aligned; fully
+ *               written (zero rows for empty sequences).
+ *  ws           see paged_gqa_workspace; NULL selects the unsplit route.
+ * Two kernels are launched on the split route (split, then merge), one on
+ * the unsplit route.  Results are deterministic for a given device, shape and
+ * force_splits: no floating-point atomics are used.
+ */
+int paged_gqa_decode(const void* q, const void* k_cache, const void* v_cache,
+                     paged_gqa_kv_layout kv_layout, int kv_dtype,
+                     const int32_t* block_table, int64_t bt_row_stride,
+                     const int32_t* seq_lens,
+                     int B, int Hq, int Hkv, int D, int page_size, int num_pages,
+                     int max_seq_len, float kv_scale, float softmax_scale,
+                     void* out, const paged_gqa_workspace* ws, void* stream);
+
+/*
+ * Selected-sparse prefill over four-token blocks of one sequence ("[Kernel]
+ * [SM70] Accelerate Qwen3.8 QSA paged prefill", Changes).  For query row r
+ * with p = min(q_pos[r], kv_len - 1) and own = p / 4, the row attends to
+ *     { 4b .. 4b+3 : b in sel_idx[r, :], 0 <= b < own }   (selected blocks)
+ *  ++ { 4*own .. p }                                      (causal tail, last)
+ * read in place from the page_size-token pages through block_table, and
+ *     out[r, h, :] = sum_t softmax_t(softmax_scale * <q[r,h,:], K_t>) V_t.
+ *
+ *  q            device, binary16 [R, Hq, D] contiguous.
+ *  k_cache,     device pools as for decode (FP16 or E4M3).
+ *  v_cache
+ *  block_table  device int32 [>= ceil(kv_len / page_size)], this sequence's pages.
+ *  sel_idx      device int32 [R, n_sel]; entries < 0 are padding; entries >=
+ *               own are skipped (PAGED_GQA_FLAG_BAD_SEL).  Order is free.
+ *  q_pos        device int32 [R]; q_pos < 0 gives a zero row
+ *               (PAGED_GQA_FLAG_EMPTY_ROW); q_pos >= kv_len is clamped
+ *               (PAGED_GQA_FLAG_QPOS_CLAMPED).
+ *  page_size    a multiple of 4, so a four-token block never straddles pages.
+ *  out          device, binary16 [R, Hq, D] contiguous; fully written.
+ * One kernel is launched; no workspace is needed.
+ */
+int paged_gqa_sparse_prefill(const void* q, const void* k_cache, const void* v_cache,
+                             paged_gqa_kv_layout kv_layout, int kv_dtype,
+                             const int32_t* block_table, int num_pages, int kv_len,
+                             const int32_t* sel_idx, int n_sel, const int32_t* q_pos,
+                             int R, int Hq, int Hkv, int D, int page_size,
+                             float kv_scale, float softmax_scale,
+                             void* out, int* err_flag, void* stream);
+
+/*
+ * Inspection: the rows the decode kernels gather, dequantised.  For every
+ * b < B, t < T and KV head j writes out[b, t, j, :] (float32, device,
+ * [B, T, Hkv, D]) = the stored row of logical token t of sequence b as a
+ * float (E4M3 code value times kv_scale, rounded once; FP16 exactly), or
+ * zeros when t >= min(seq_lens[b], max_seq_len) or its page is invalid.  Uses
+ * the decode kernels' own address arithmetic and E4M3 converter, so tests can
+ * compare the gather and the dequantisation bit for bit.
+ */
+int paged_gqa_gather_dequant(const void* cache, paged_gqa_kv_layout kv_layout, int kv_dtype,
+                             const int32_t* block_table, int64_t bt_row_stride,
+                             const int32_t* seq_lens, int B, int T, int Hkv, int D,
+                             int page_size, int num_pages, int max_seq_len, float kv_scale,
+                             float* out, void* stream);
+
+/*
+ * Inspection: the token list the sparse-prefill kernel builds for each row.
+ * out is device int32 [R, 4 * (n_sel + 1)]: slot 4*i + u holds the logical
+ * token of lane u of block entry i (entries 0..n_sel-1 are sel_idx[r, i],
+ * entry n_sel is the row's causal tail block), or -1 when that slot is not
+ * attended.  Uses the prefill kernel's own index arithmetic.
+ */
+int paged_gqa_sparse_prefill_tokens(const int32_t* block_table, int num_pages, int kv_len,
+                                    const int32_t* sel_idx, int n_sel, const int32_t* q_pos,
+                                    int R, int page_size, int32_t* out, void* stream);
+
+/* Human-readable name of a status code (static string). */
+const char* paged_gqa_status_string(int status);
+
+/* PAGED_GQA_VERSION of the loaded library. */
+int paged_gqa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGED_GQA_H */

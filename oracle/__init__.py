@@ -167,7 +167,9 @@ class Oracle:
         Hkv = k.shape[2]
         ps, ts, hs = _kv_strides(k, v)
         bt = np.ascontiguousarray(block_table, dtype=np.int32).reshape(-1)
-        sel = np.ascontiguousarray(sel_idx, dtype=np.int32).reshape(R, -1)
+        sel = np.ascontiguousarray(sel_idx, dtype=np.int32)
+        if sel.ndim != 2 or sel.shape[0] != R:
+            raise ValueError("sel_idx must be [R, n_sel]")
         qp = np.ascontiguousarray(q_pos, dtype=np.int32)
         out = np.zeros((R, Hq, D), dtype=np.float16)
         o64 = np.zeros((R, Hq, D), dtype=np.float64) if want_f64 else None
