@@ -20,10 +20,11 @@ def _built():
     __graft_entry__.build()
 
 
-def _check_full(case, **kw):
+def _check_full(case, strict=False, **kw):
     got, flags = U.run_decode(case, **kw)
     want, _, oflags = U.oracle_decode(case)
-    U.assert_close(got, want, case.name)
+    _, _, wide = U.assert_close(got, want, case.name)
+    assert not (strict and wide), f"{case.name}: {wide} elements needed the ULP allowance"
     assert flags == oflags, f"{case.name}: flags {flags} != oracle {oflags}"
     return got
 
@@ -32,7 +33,8 @@ def _check_pairs(case, pairs, kv=None, **kw):
     got, flags = U.run_decode(case, kv=kv, **kw)
     want, _, oflags = U.oracle_decode(case, pairs=pairs)
     b, h = pairs[:, 0], pairs[:, 1]
-    U.assert_close(got[b, h], want[b, h], case.name)
+    _, _, wide = U.assert_close(got[b, h], want[b, h], case.name)
+    assert wide == 0, f"{case.name}: {wide} elements needed the ULP allowance"
     assert flags == oflags
     return got
 
@@ -41,13 +43,13 @@ def _check_pairs(case, pairs, kv=None, **kw):
 
 def test_tiny_fp16_split_and_unsplit():
     c = W.tiny_fp16()
-    a = _check_full(c)
-    b = _check_full(c, workspace=False)
+    a = _check_full(c, strict=True)
+    b = _check_full(c, strict=True, workspace=False)
     U.assert_close(a, b, "split vs unsplit")
 
 
 def test_e4m3_b8():
-    _check_full(W.e4m3_b8())
+    _check_full(W.e4m3_b8(), strict=True)
 
 
 @pytest.fixture(scope="module")
@@ -67,7 +69,7 @@ def test_long_e4m3_sampled(long_case):
 def test_sweep(B, L, kvd):
     c = W.sweep(B, L, kvd)
     if L == 1024:
-        _check_full(c)
+        _check_full(c, strict=True)
     else:
         _check_pairs(c, U.sample_pairs(B, c.Hq, per_seq=2, seed=B))
 
