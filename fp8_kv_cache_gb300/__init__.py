@@ -26,7 +26,8 @@ import threading
 __all__ = [
     "PagedGQAError", "library_path", "lib", "KV_FP16", "KV_E4M3",
     "FLAG_BAD_PAGE", "FLAG_SEQ_CLAMPED", "FLAG_EMPTY_ROW", "FLAG_QPOS_CLAMPED", "FLAG_BAD_SEL",
-    "paged_gqa_decode", "paged_gqa_sparse_prefill", "paged_gqa_gather_dequant",
+    "paged_gqa_decode", "paged_gqa_decode_noalloc", "paged_gqa_sparse_prefill",
+    "paged_gqa_gather_dequant",
     "paged_gqa_sparse_prefill_tokens", "paged_gqa_decode_workspace_size",
     "paged_gqa_decode_workspace_size_splits",
     "paged_gqa_status_string", "paged_gqa_version", "Workspace",
@@ -89,6 +90,10 @@ def lib():
                                            i32, i32, i32, i32, i32, i32, i32, f32, f32,
                                            vp, ctypes.POINTER(Workspace), vp]
             L.paged_gqa_decode.restype = i32
+            L.paged_gqa_decode_noalloc.argtypes = [vp, vp, vp, KVLayout, i32, vp, i64, vp,
+                                                   i32, i32, i32, i32, i32, i32, i32, f32, f32,
+                                                   vp, vp, vp]
+            L.paged_gqa_decode_noalloc.restype = i32
             L.paged_gqa_sparse_prefill.argtypes = [vp, vp, vp, KVLayout, i32, vp, i32, i32,
                                                    vp, i32, vp, i32, i32, i32, i32, i32, f32, f32,
                                                    vp, vp, vp]
@@ -203,6 +208,29 @@ def paged_gqa_decode(q, k_cache, v_cache, block_table, seq_lens, page_size, kv_s
         B, Hq, Hkv, D, page_size, num_pages, max_seq_len, float(kv_scale), float(softmax_scale),
         _ptr(out), ctypes.byref(ws), _stream(stream))
     _check(st, "paged_gqa_decode")
+    return out
+
+
+def paged_gqa_decode_noalloc(q, k_cache, v_cache, block_table, seq_lens, page_size, kv_scale,
+                             softmax_scale, out=None, *, max_seq_len, num_pages=None,
+                             err_flag=None, stream=None):
+    """paged_gqa_decode for callers that cannot allocate device memory: the
+    split scratch is the library's own 16 MiB static device array, so the
+    call allocates nothing (``out`` is allocated here only when not given).
+    Calls that may overlap on the GPU share that array and race; the first
+    call on a device should precede any stream capture."""
+    torch = _torch()
+    B, Hq, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if num_pages is None:
+        num_pages = k_cache.shape[0]
+    st = lib().paged_gqa_decode_noalloc(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _layout(k_cache, v_cache), _kv_dtype(k_cache),
+        _ptr(block_table), block_table.stride(0), _ptr(seq_lens),
+        B, Hq, k_cache.shape[2], D, page_size, num_pages, max_seq_len, float(kv_scale),
+        float(softmax_scale), _ptr(out), _ptr(err_flag), _stream(stream))
+    _check(st, "paged_gqa_decode_noalloc")
     return out
 
 

@@ -147,6 +147,36 @@ int paged_gqa_decode(const void* q, const void* k_cache, const void* v_cache,
                      void* out, const paged_gqa_workspace* ws, void* stream);
 
 /*
+ * paged_gqa_decode for callers that cannot allocate device memory.  The
+ * pages have no counterpart of this entry point; it exists for users of this
+ * library whose code runs where a cudaMalloc is forbidden or unwanted (an
+ * execute hook of a host framework that owns all device memory, a
+ * latency-critical path where an allocation could synchronise the device, a
+ * process whose memory another allocator already holds).
+ *
+ * Same arguments and results as paged_gqa_decode with the split route, except
+ * that there is no workspace argument: the split scratch lives in a 16 MiB
+ * static device array inside this library (held on every GPU that loads the
+ * library until the process exits) and the call allocates nothing.  err_flag
+ * is the optional device int of PAGED_GQA_FLAG_* bits.
+ *  * Shapes whose scratch exceeds 16 MiB (paged_gqa_decode_workspace_size()
+ *    above 16777216 bytes) are refused with PAGED_GQA_ERR_WORKSPACE before
+ *    anything is launched.
+ *  * The first call on each device looks up the array's device address with
+ *    that device current; make that first call before any stream capture.
+ *  * Every call shares the array: calls whose kernels may overlap on the GPU
+ *    (e.g. on unordered streams) race and give wrong results; calls ordered
+ *    on one stream are safe.  No scratch value needs to start at zero.
+ */
+int paged_gqa_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                             paged_gqa_kv_layout kv_layout, int kv_dtype,
+                             const int32_t* block_table, int64_t bt_row_stride,
+                             const int32_t* seq_lens,
+                             int B, int Hq, int Hkv, int D, int page_size, int num_pages,
+                             int max_seq_len, float kv_scale, float softmax_scale,
+                             void* out, int* err_flag, void* stream);
+
+/*
  * Selected-sparse prefill over four-token blocks of one sequence ("[Kernel]
  * [SM70] Accelerate Qwen3.8 QSA paged prefill", Changes).  For query row r
  * with p = min(q_pos[r], kv_len - 1) and own = p / 4, the row attends to
