@@ -159,6 +159,8 @@ def run_ours(args, rank, world):
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
 
+    if args.phase == "prefill":
+        return run_prefill_only(args, dev)
     case = W.long_e4m3()
     kvb = decode_kv_bytes(case)
     kv = torch.from_numpy(case.kv).to(dev)
@@ -210,6 +212,11 @@ def run_ours(args, rank, world):
         total_ms = float(t.item())
     ms_per_step = total_ms / K
     value = world * kvb * K / (total_ms * 1e-3) / 1e9
+
+    if args.phase == "decode":
+        clocks.stop()
+        return {"phase": "decode", "ms_per_step": total_ms / K,
+                "split_ms": float(np.mean(split_ms)), "value": value}
 
     # ---- end to end: per-step inputs from pinned host memory, result back
     q_h = torch.from_numpy(case.q).pin_memory()
@@ -330,6 +337,32 @@ def run_ours(args, rank, world):
     return line
 
 
+def run_prefill_only(args, dev):
+    """The sparse-prefill phase alone (for profiling)."""
+    import torch
+    import fp8_kv_cache_gb300 as P
+    from fp8_kv_cache_gb300 import workloads as W
+    pc = W.sparse_prefill_4096()
+    pkv = torch.from_numpy(pc.kv).to(dev)
+    pk, pv = pkv[:, :, :, 0, :], pkv[:, :, :, 1, :]
+    pq = torch.from_numpy(pc.q).to(dev)
+    pbt = torch.from_numpy(pc.block_table).to(dev)
+    psel = torch.from_numpy(pc.sel_idx).to(dev)
+    ppos = torch.from_numpy(pc.q_pos).to(dev)
+    pout = torch.empty_like(pq)
+    ms = []
+    for i in range(args.warmup + args.steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        P.paged_gqa_sparse_prefill(pq, pk, pv, pbt, pc.kv_len, psel, ppos, pc.page_size,
+                                   pc.softmax_scale, pc.kv_scale, pout)
+        b.record()
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            ms.append(a.elapsed_time(b))
+    return {"phase": "prefill", "ms": float(np.mean(ms))}
+
+
 def cpu_baseline(sample_seqs=4, threads=None):
     """The FP64 oracle on the first ``sample_seqs`` sequences of the decode
     workload, all heads; returns (GB/s-equivalent of KV processed, dict)."""
@@ -398,6 +431,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--phase", choices=["all", "decode", "prefill"], default="all",
+                    help="run only one phase (for profiling); the JSON line needs 'all'")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -415,7 +450,7 @@ def main():
         dist.init_process_group("nccl")
     line = run_ours(args, rank, world)
     if rank == 0:
-        if not args.no_cpu_baseline:
+        if not args.no_cpu_baseline and args.phase == "all":
             _, line["cpu_baseline"] = cpu_baseline()
         print(json.dumps(line), flush=True)
     if world > 1:

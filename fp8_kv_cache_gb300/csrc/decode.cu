@@ -45,31 +45,28 @@ __device__ __forceinline__ int find_seq(const int64_t* P, int B, int Hkv, int64_
 // half-tiles of 8 tokens, round-robin), then merged into out_rows (final) or
 // slot (partial).
 template <bool kE4M3>
-__device__ void run_piece(const DecodeArgs& a, MergeSmem& sm, int b, int j, int L, int ta,
+__device__ void run_piece(const DecodeArgs& a, const CtaSmem<kE4M3>& cs,
+                          WarpRing<kE4M3, kStages<kE4M3>()>& rg, int b, int j, int L, int ta,
                           int te, __half* out_rows, float* slot, int& flags)
 {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const int g = lane >> 2, q = lane & 3;
+    const int g = lane >> 2;
     using Core = WarpCore<kE4M3>;
-    uint2* qs = q_stage(sm, w);
-    Core::stage_q(qs, a.q + ((size_t)b * a.Hq + (size_t)j * a.G) * kD, a.G, lane);
+    Core::stage_q(cs.qs, a.q + ((size_t)b * a.Hq + (size_t)j * a.G) * kD, a.G, lane);
     Core wc;
     wc.reset();
     const int32_t* bt_row = a.bt + (int64_t)b * a.bt_stride;
-    auto offsets = [&](int h, int64_t& ok, int64_t& o0, int64_t& o1) {
-        int64_t off = -1;
+    auto offset = [&](int h) -> int64_t {
         if (lane < kHalf) {
             const int t = h * kHalf + lane;
             if (t < L)
-                off = token_row_offset(a.kv, bt_row, t, j, flags);
+                return token_row_offset(a.kv, bt_row, t, j, flags);
         }
-        ok = __shfl_sync(0xffffffffu, off, g);
-        o0 = __shfl_sync(0xffffffffu, off, 2 * q);
-        o1 = __shfl_sync(0xffffffffu, off, 2 * q + 1);
+        return -1;
     };
-    run_halves<kE4M3, kRing<kE4M3>()>(wc, qs, a.kv.k, a.kv.v, 2 * ta + w, 2 * te, kWarps,
-                                      g < a.G, a.scale_log2, lane, offsets);
-    cta_merge<kE4M3>(sm, wc, a.G, a.v_scale, out_rows, slot);
+    run_halves<kE4M3, kStages<kE4M3>()>(wc, rg, cs.qs, a.kv.k, a.kv.v, 2 * ta + w, 2 * te, kWarps,
+                                        g < a.G, a.scale_log2, lane, offset);
+    cta_merge<kE4M3>(*cs.merge, wc, a.G, a.v_scale, out_rows, slot);
 }
 
 __device__ void zero_rows(__half* rows, int G)
@@ -83,9 +80,13 @@ __device__ void zero_rows(__half* rows, int G)
 template <bool kE4M3>
 __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(DecodeArgs a)
 {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    MergeSmem& sm = *reinterpret_cast<MergeSmem*>(smem_raw);
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    const CtaSmem<kE4M3> cs = CtaSmem<kE4M3>::carve(smem_raw, threadIdx.x >> 5);
+    WarpRing<kE4M3, kStages<kE4M3>()> rg;
+    rg.init(cs.ring, cs.masks);
     int flags = 0;
+    // The merge kernel may be scheduled now; it waits for this grid's results.
+    asm volatile("griddepcontrol.launch_dependents;");
 
     if (a.C == 0) {
         // ---- unsplit route: CTA = one whole segment
@@ -101,14 +102,15 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(DecodeArgs a)
         if (L == 0) {
             zero_rows(out_rows, a.G);
         } else {
-            run_piece<kE4M3>(a, sm, b, j, L, 0, (L + kTile - 1) / kTile, out_rows, nullptr, flags);
+            run_piece<kE4M3>(a, cs, rg, b, j, L, 0, (L + kTile - 1) / kTile, out_rows, nullptr,
+                             flags);
         }
         raise_flag(a.err, flags);
         return;
     }
 
     // ---- split route: exclusive prefix P[b] of per-sequence tile counts
-    int64_t* P = reinterpret_cast<int64_t*>(smem_raw + sizeof(MergeSmem));
+    int64_t* P = reinterpret_cast<int64_t*>(cs.tail);
     int64_t* wtot = P + (a.B + 1);
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const int per = (a.B + kThreads - 1) / kThreads;
@@ -181,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(DecodeArgs a)
         const bool whole = x0 <= s0 && x1 >= s1;
         __half* out_rows = whole ? a.out + ((size_t)b * a.Hq + (size_t)j * a.G) * kD : nullptr;
         float* slot = whole ? nullptr : a.slots + (size_t)(c + k) * kSlotFloats;
-        run_piece<kE4M3>(a, sm, b, j, L, ta, te, out_rows, slot, flags);
+        run_piece<kE4M3>(a, cs, rg, b, j, L, ta, te, out_rows, slot, flags);
         // next non-empty segment
         if (++j == a.Hkv) {
             j = 0;
@@ -196,18 +198,25 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(DecodeArgs a)
     raise_flag(a.err, flags);
 }
 
-// One CTA per segment (grid Hkv x B): zero rows for empty segments, nothing
-// for segments one split CTA covered, else the fixed-order LSE merge
+// One CTA per (query head h, sequence b) (grid Hq x B, 64 threads, four
+// head-dim values each): zero rows for empty sequences, nothing for segments
+// one split CTA covered, else the fixed-order LSE merge of the pieces
 //   M = max m_i,  O = sum_i 2^(m_i - M) O_i / sum_i 2^(m_i - M) l_i.
+// Launched as a programmatic dependent of the split kernel: it may start
+// early and waits on griddepcontrol.wait for the split kernel's results.
 __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeArgs a)
 {
-    const int j = blockIdx.x, b = blockIdx.y;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int h = blockIdx.x, b = blockIdx.y;
+    const int j = h / a.G, hh = h - j * a.G;
+    const int d = 4 * threadIdx.x;
     const int64_t T = a.hdr[0], C = a.hdr[1];
     const int64_t* P = a.hdr + 2;
     const int64_t nb = P[b + 1] - P[b];
-    __half* out_rows = a.out + ((size_t)b * a.Hq + (size_t)j * a.G) * kD;
+    __half2* out2 = reinterpret_cast<__half2*>(a.out + ((size_t)b * a.Hq + h) * kD + d);
     if (nb == 0) {
-        zero_rows(out_rows, a.G);
+        out2[0] = __floats2half2_rn(0.f, 0.f);
+        out2[1] = __floats2half2_rn(0.f, 0.f);
         return;
     }
     const int64_t s0 = (int64_t)a.Hkv * P[b] + (int64_t)j * nb;
@@ -217,32 +226,37 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeArgs 
     if (c_first == c_last)
         return;
     const int64_t k = (int64_t)b * a.Hkv + j;
-    const int d = threadIdx.x;
     // CTAs with an empty tile range (possible when C > T) wrote no slot.
     auto empty = [&](int64_t c) { return c * T / C == (c + 1) * T / C; };
-    for (int h = 0; h < a.G; ++h) {
-        float M = -INFINITY;
-        for (int64_t c = c_first; c <= c_last; ++c)
-            if (!empty(c))
-                M = fmaxf(M, a.slots[(size_t)(c + k) * kSlotFloats + h]);
-        float num = 0.f, den = 0.f;
-        if (M != -INFINITY) {
-            for (int64_t c = c_first; c <= c_last; ++c) {
-                if (empty(c))
-                    continue;
-                const float* sl = a.slots + (size_t)(c + k) * kSlotFloats;
-                const float e = ex2(sl[h] - M);
-                den += e * sl[kGMax + h];
-                num += e * sl[2 * kGMax + h * kD + d];
-            }
+    float M = -INFINITY;
+    for (int64_t c = c_first; c <= c_last; ++c)
+        if (!empty(c))
+            M = fmaxf(M, a.slots[(size_t)(c + k) * kSlotFloats + hh]);
+    float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+    float den = 0.f;
+    if (M != -INFINITY) {
+        for (int64_t c = c_first; c <= c_last; ++c) {
+            if (empty(c))
+                continue;
+            const float* sl = a.slots + (size_t)(c + k) * kSlotFloats;
+            const float e = ex2(sl[hh] - M);
+            den += e * sl[kGMax + hh];
+            const float4 o = *reinterpret_cast<const float4*>(sl + 2 * kGMax + hh * kD + d);
+            num.x += e * o.x;
+            num.y += e * o.y;
+            num.z += e * o.z;
+            num.w += e * o.w;
         }
-        out_rows[(size_t)h * kD + d] = __float2half_rn(den > 0.f ? num / den * a.v_scale : 0.f);
     }
+    const float sc = den > 0.f ? a.v_scale / den : 0.f;
+    out2[0] = __floats2half2_rn(num.x * sc, num.y * sc);
+    out2[1] = __floats2half2_rn(num.z * sc, num.w * sc);
 }
 
-size_t decode_split_smem(int B)
+size_t decode_split_smem(bool e4m3, int B)
 {
-    return sizeof(MergeSmem) + (size_t)(B + 1) * sizeof(int64_t) + kWarps * sizeof(int64_t);
+    const size_t tail = (size_t)(B + 1) * sizeof(int64_t) + kWarps * sizeof(int64_t);
+    return (e4m3 ? SmemPlan<true>::kTailOff : SmemPlan<false>::kTailOff) + tail;
 }
 
 size_t workspace_bytes(int B, int Hkv, int C)
@@ -265,7 +279,7 @@ static cudaError_t set_smem_attr()
     if (dev < kMaxDevices && done[dev].load(std::memory_order_acquire))
         return cudaSuccess;
     e = cudaFuncSetAttribute(decode_split_kernel<kE4M3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)decode_split_smem(kMaxSplitBatch));
+                             (int)decode_split_smem(kE4M3, kMaxSplitBatch));
     if (e == cudaSuccess && dev < kMaxDevices)
         done[dev].store(1, std::memory_order_release);
     return e;
@@ -274,7 +288,7 @@ static cudaError_t set_smem_attr()
 int split_ctas_per_sm(bool e4m3)
 {
     int n = 0;
-    const size_t smem = decode_split_smem(64);
+    const size_t smem = decode_split_smem(e4m3, 64);
     cudaError_t e = e4m3 ? set_smem_attr<true>() : set_smem_attr<false>();
     if (e != cudaSuccess)
         return 1;
@@ -291,7 +305,8 @@ cudaError_t launch_decode(const DecodeArgs& a, bool e4m3, cudaStream_t s, void* 
     if (e != cudaSuccess)
         return e;
     const int grid = a.C > 0 ? a.C : a.B * a.Hkv;
-    const size_t smem = a.C > 0 ? decode_split_smem(a.B) : sizeof(MergeSmem);
+    const size_t smem = a.C > 0 ? decode_split_smem(e4m3, a.B)
+                                : (e4m3 ? SmemPlan<true>::kTailOff : SmemPlan<false>::kTailOff);
     if (ev0 && ev1 && (e = cudaEventRecord((cudaEvent_t)ev0, s)) != cudaSuccess)
         return e;
     if (e4m3)
@@ -303,8 +318,17 @@ cudaError_t launch_decode(const DecodeArgs& a, bool e4m3, cudaStream_t s, void* 
     if (ev0 && ev1 && (e = cudaEventRecord((cudaEvent_t)ev1, s)) != cudaSuccess)
         return e;
     if (a.C > 0) {
-        decode_merge_kernel<<<dim3(a.Hkv, a.B), kMergeThreads, 0, s>>>(a);
-        if ((e = cudaGetLastError()) != cudaSuccess)
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(a.Hq, a.B);
+        cfg.blockDim = dim3(kMergeThreads);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if ((e = cudaLaunchKernelEx(&cfg, decode_merge_kernel, a)) != cudaSuccess)
             return e;
     }
     return cudaSuccess;

@@ -177,25 +177,6 @@ struct HalfTile {
     uint4 k[kKCh];
     uint4 v[2][kVCh];
     bool valid[2];                               // tokens 2q, 2q+1 attended
-
-    // Loads given the byte offsets of the three rows (< 0: not attended,
-    // registers zeroed so that masked tokens never read memory).
-    __device__ void load(const unsigned char* kbase, const unsigned char* vbase, int64_t ok,
-                         int64_t ov0, int64_t ov1, int g, int q)
-    {
-#pragma unroll
-        for (int i = 0; i < kKCh; ++i)
-            k[i] = ok >= 0 ? ldg_stream(kbase + ok + 16 * (q + 4 * i)) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const int64_t o = u ? ov1 : ov0;
-#pragma unroll
-            for (int i = 0; i < kVCh; ++i)
-                v[u][i] = o >= 0 ? ldg_stream(vbase + o + 16 * g + 128 * i) : make_uint4(0, 0, 0, 0);
-        }
-        valid[0] = ov0 >= 0;
-        valid[1] = ov1 >= 0;
-    }
 };
 
 // Register-resident attention state of one warp for one (sequence or row,
@@ -315,43 +296,210 @@ struct WarpCore {
     }
 };
 
-// Runs a warp over half-tiles h = first, first + stride, ... < end with a
-// register ring of kNB buffers (kNB - 1 half-tiles in flight while one is
-// computed).  offsets(h, ok, ov0, ov1) gives the three row offsets of
-// half-tile h for this lane.
-template <bool kE4M3, int kNB, class Offsets>
-__device__ __forceinline__ void run_halves(WarpCore<kE4M3>& wc, const uint2* qs,
-                                           const unsigned char* kb, const unsigned char* vb,
-                                           int first, int end, int stride, bool head_ok,
-                                           float scale_log2, int lane, Offsets offsets)
+// ------------------------------------------------------------------ async ring
+
+// One stage of a warp's shared-memory ring holds one half-tile: the K rows of
+// its 8 tokens, then their V rows.  Row strides are padded so that the
+// fragment reads below are free of bank conflicts: a K row is read by lanes
+// (g, q) as chunks q + 4i (8 rows x 4 chunks per quarter-warp phase -> the
+// stride must be 64 mod 128 bytes); a V row pair 2q, 2q+1 is read at chunk
+// g + 8i (stride 16 mod 64 bytes).
+template <bool kE4M3>
+struct Stage {
+    static constexpr int kRowBytes = kE4M3 ? 256 : 512;
+    static constexpr int kKStride = kRowBytes + 64;
+    static constexpr int kVStride = kRowBytes + 16;
+    static constexpr int kKBytes = kHalf * kKStride;
+    static constexpr int kBytes = kHalf * (kKStride + kVStride);
+};
+
+// Ring depth (stages per warp): kNS - 1 half-tiles stay in flight while one
+// is read.  Chosen so that two CTAs of four warps fit on one SM.
+template <bool kE4M3>
+__host__ __device__ constexpr int kStages()
+{
+    return kE4M3 ? 4 : 2;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr)
+{
+    uint4 r;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "r"(addr));
+    return r;
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const unsigned char* src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit()
+{
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// A warp's private ring of kNS stages filled by 16-byte asynchronous copies
+// (global -> shared, bypassing L1).  Each fill is one commit group per lane;
+// a stage is ready once every lane's group for it has completed and the warp
+// has synchronised.  The same warp produces and consumes, so no CTA-wide
+// synchronisation is involved, and completion needs no waiting loop.
+template <bool kE4M3, int kNS>
+struct WarpRing {
+    uint32_t ring;        // shared address of stage 0
+    uint32_t* masks;      // kNS words: bit t = token t of the stage is valid
+
+    __device__ void init(unsigned char* ring_ptr, uint32_t* mask_ptr)
+    {
+        ring = smem_u32(ring_ptr);
+        masks = mask_ptr;
+    }
+
+    // Starts filling stage s and commits one group.  Lane t < 8 passes the
+    // byte offset of token t's rows (K and V share it), or < 0 when the token
+    // is not attended.  Chunk c of a row is copied by lane c (FP16 rows are
+    // 32 chunks) or lane c + 16 * (row parity) (E4M3 rows are 16 chunks), so
+    // every copy instruction reads whole 512-byte row pieces.
+    __device__ void fill(int s, int64_t off, const unsigned char* kb, const unsigned char* vb,
+                         int lane)
+    {
+        using St = Stage<kE4M3>;
+        const uint32_t mask = __ballot_sync(0xffffffffu, lane < kHalf && off >= 0) & 0xFFu;
+        if (lane == 0)
+            masks[s] = mask;
+        const uint32_t base = ring + s * St::kBytes;
+        if (kE4M3) {
+            // instruction k: token 2(k % 4) + lane / 16, chunk lane % 16, K for k < 4
+            const int half = lane >> 4, c = lane & 15;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int t = 2 * k + half;
+                const int64_t o = __shfl_sync(0xffffffffu, off, t);
+                if ((mask >> t) & 1u) {
+                    cp_async16(base + t * St::kKStride + 16 * c, kb + o + 16 * c);
+                    cp_async16(base + St::kKBytes + t * St::kVStride + 16 * c, vb + o + 16 * c);
+                }
+            }
+        } else {
+            // instruction k: token k, chunk lane
+#pragma unroll
+            for (int t = 0; t < kHalf; ++t) {
+                const int64_t o = __shfl_sync(0xffffffffu, off, t);
+                if ((mask >> t) & 1u) {
+                    cp_async16(base + t * St::kKStride + 16 * lane, kb + o + 16 * lane);
+                    cp_async16(base + St::kKBytes + t * St::kVStride + 16 * lane, vb + o + 16 * lane);
+                }
+            }
+        }
+        cp_async_commit();
+    }
+
+    // Commits an empty group (keeps one group per ring slot).
+    __device__ void skip() const
+    {
+        cp_async_commit();
+    }
+
+    // The oldest of the kNS - 1 committed fills is complete for every lane
+    // (at most kNS - 2 groups may still be pending).
+    __device__ void wait() const
+    {
+        static_assert(kNS >= 2, "the ring needs at least two stages");
+        cp_async_wait<kNS - 2>();
+        __syncwarp();
+    }
+
+    __device__ void drain() const
+    {
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        __syncwarp();
+    }
+
+    // The fragments lane (g, q) needs from stage s: K row g, V rows 2q, 2q+1
+    // (zeros for tokens that are not attended).
+    __device__ void read(int s, HalfTile<kE4M3>& t, int g, int q) const
+    {
+        using St = Stage<kE4M3>;
+        const uint32_t mask = masks[s];
+        const uint32_t base = ring + s * St::kBytes;
+        const bool kv = (mask >> g) & 1u;
+#pragma unroll
+        for (int i = 0; i < HalfTile<kE4M3>::kKCh; ++i)
+            t.k[i] = kv ? lds128(base + g * St::kKStride + 16 * (q + 4 * i)) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int row = 2 * q + u;
+            const bool vv = (mask >> row) & 1u;
+            t.valid[u] = vv;
+#pragma unroll
+            for (int i = 0; i < HalfTile<kE4M3>::kVCh; ++i)
+                t.v[u][i] = vv ? lds128(base + St::kKBytes + row * St::kVStride + 16 * g + 128 * i)
+                               : make_uint4(0, 0, 0, 0);
+        }
+    }
+};
+
+// Runs a warp over half-tiles h = first, first + stride, ... < end through
+// its ring: kNS - 1 fills in flight; per half-tile: wait for the oldest fill,
+// read its fragments, refill that stage kNS - 1 half-tiles ahead, compute.
+// offset(h) returns, on lanes t < 8, the byte offset of token t of half-tile h
+// (or -1), and -1 on the other lanes.
+template <bool kE4M3, int kNS, class Offset>
+__device__ __forceinline__ void run_halves(WarpCore<kE4M3>& wc, WarpRing<kE4M3, kNS>& rg,
+                                           const uint2* qs, const unsigned char* kb,
+                                           const unsigned char* vb, int first, int end, int stride,
+                                           bool head_ok, float scale_log2, int lane, Offset offset)
 {
     const int g = lane >> 2, q = lane & 3;
-    HalfTile<kE4M3> buf[kNB];
-#pragma unroll
-    for (int u = 0; u < kNB - 1; ++u) {
-        const int h = first + u * stride;
-        if (h < end) {
-            int64_t ok, o0, o1;
-            offsets(h, ok, o0, o1);
-            buf[u].load(kb, vb, ok, o0, o1, g, q);
-        }
+    const int n = end > first ? (end - first + stride - 1) / stride : 0;
+    if (n == 0)
+        return;
+    for (int i = 0; i < kNS - 1; ++i) {
+        if (i < n)
+            rg.fill(i, offset(first + i * stride), kb, vb, lane);
+        else
+            rg.skip();
     }
-    for (int base = first; base < end; base += kNB * stride) {
-#pragma unroll
-        for (int u = 0; u < kNB; ++u) {
-            const int h = base + u * stride;
-            if (h >= end)
-                break;
-            const int hn = h + (kNB - 1) * stride;
-            if (hn < end) {
-                int64_t ok, o0, o1;
-                offsets(hn, ok, o0, o1);
-                buf[(u + kNB - 1) % kNB].load(kb, vb, ok, o0, o1, g, q);
-            }
-            wc.step(buf[u], qs, head_ok, scale_log2, lane);
-        }
+    for (int i = 0; i < n; ++i) {
+        const int s = i % kNS;
+        HalfTile<kE4M3> t;
+        rg.wait();
+        rg.read(s, t, g, q);
+        __syncwarp();
+        const int nf = i + kNS - 1;
+        if (nf < n)
+            rg.fill(nf % kNS, offset(first + nf * stride), kb, vb, lane);
+        else
+            rg.skip();
+        wc.step(t, qs, head_ok, scale_log2, lane);
     }
+    rg.drain();
 }
+
+// Shared-memory carve-up of a CTA of the attention kernels:
+//   [Q fragments of 4 warps][rings of 4 warps (the merge buffer aliases them)]
+//   [stage masks][kernel-specific tail]
+template <bool kE4M3>
+struct SmemPlan {
+    static constexpr int kNS = kStages<kE4M3>();
+    static constexpr size_t kQBytes = (size_t)kWarps * 16 * 32 * sizeof(uint2);
+    static constexpr size_t kRingBytes = (size_t)kWarps * kNS * Stage<kE4M3>::kBytes;
+    static constexpr size_t kRingOrMerge = kRingBytes;   // asserted >= sizeof(MergeSmem) below
+    static constexpr size_t kMaskOff = kQBytes + kRingOrMerge;
+    static constexpr size_t kTailOff = (kMaskOff + (size_t)kWarps * kNS * 4 + 15) & ~(size_t)15;
+};
 
 // ------------------------------------------------------------------ CTA merge
 
@@ -364,19 +512,28 @@ struct MergeSmem {
     float o[kWarps][kGMax][kD];
 };
 
-// Q fragments of warp w (16 x 32 uint2 = 4 KB), staged in the merge buffer:
-// cta_merge starts and ends with a CTA barrier, so the two uses never overlap.
-__device__ __forceinline__ uint2* q_stage(MergeSmem& sm, int w)
-{
-    return reinterpret_cast<uint2*>(&sm.o[0][0][0]) + w * 16 * 32;
-}
-
-// Half-tiles in the register ring: kRing - 1 are in flight while one is used.
+// The pieces of a CTA's shared memory for one attention kernel instance.
 template <bool kE4M3>
-__host__ __device__ constexpr int kRing()
-{
-    return kE4M3 ? 2 : 1;
-}
+struct CtaSmem {
+    uint2* qs;            // this warp's Q fragments
+    MergeSmem* merge;     // aliases the rings; used only after every ring is drained
+    unsigned char* ring;  // this warp's ring
+    uint32_t* masks;      // this warp's stage masks
+    unsigned char* tail;  // kernel-specific tail
+
+    __device__ static CtaSmem carve(unsigned char* base, int w)
+    {
+        using Pl = SmemPlan<kE4M3>;
+        static_assert(Pl::kRingBytes >= sizeof(MergeSmem), "merge buffer must fit in the rings");
+        CtaSmem c;
+        c.qs = reinterpret_cast<uint2*>(base) + w * 16 * 32;
+        c.merge = reinterpret_cast<MergeSmem*>(base + Pl::kQBytes);
+        c.ring = base + Pl::kQBytes + (size_t)w * Pl::kNS * Stage<kE4M3>::kBytes;
+        c.masks = reinterpret_cast<uint32_t*>(base + Pl::kMaskOff) + w * Pl::kNS;
+        c.tail = base + Pl::kTailOff;
+        return c;
+    }
+};
 
 template <bool kE4M3>
 __device__ void cta_merge(MergeSmem& sm, const WarpCore<kE4M3>& wc, int G, float v_scale,

@@ -10,7 +10,7 @@
 namespace pgqa {
 
 constexpr int kMaxSplitBatch = 4096;   // split route keeps a (B+1) prefix in shared memory
-constexpr int kMergeThreads = 256;
+constexpr int kMergeThreads = 64;     // 4 head-dim values per thread
 constexpr int kHeaderBytes = 64;       // workspace header: T, C_eff
 constexpr int kMaxDevices = 64;        // per-device caches
 
@@ -46,7 +46,7 @@ struct PrefillArgs {
     int* err;
 };
 
-size_t decode_split_smem(int B);
+size_t decode_split_smem(bool e4m3, int B);
 size_t workspace_bytes(int B, int Hkv, int C);
 int split_ctas_per_sm(bool e4m3);
 

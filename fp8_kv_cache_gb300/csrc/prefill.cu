@@ -9,12 +9,15 @@
 // plain strides here.
 //
 // Design (ours): one CTA per (query row, KV head).  Its four warps take the
-// row's 16-token tiles (four block entries each) round-robin; each lane of
-// 0..15 resolves one token (selected block id -> token -> page -> row
-// address) so the gather is done by the same register-direct tensor-core
-// pipeline as decode, then the warps merge through shared memory and the CTA
+// row's half-tiles (two block entries = 8 tokens each) round-robin; lane t of
+// 0..7 resolves token t (selected block id -> token -> page -> row address)
+// and the warp copies the K and V rows into its shared-memory ring with
+// 16-byte asynchronous copies, so the gather runs through the same tensor-core
+// pipeline as decode; the warps then merge through shared memory and the CTA
 // writes the row's FP16 outputs.  No table of virtual pages is built: the
 // four-token block addresses are computed inline.
+#include <atomic>
+
 #include "pgqa_internal.h"
 
 namespace pgqa {
@@ -22,10 +25,10 @@ namespace pgqa {
 template <bool kE4M3>
 __global__ void __launch_bounds__(kThreads, 2) sparse_prefill_kernel(PrefillArgs a)
 {
-    __shared__ MergeSmem sm;
+    extern __shared__ __align__(128) unsigned char smem_raw[];
     const int r = blockIdx.x, j = blockIdx.y;
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const int g = lane >> 2, q = lane & 3;
+    const int g = lane >> 2;
     int flags = 0;
     __half* out_rows = a.out + ((size_t)r * a.Hq + (size_t)j * a.G) * kD;
 
@@ -47,36 +50,57 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_prefill_kernel(PrefillArgs
     const int32_t* sel_row = a.sel + (size_t)r * a.n_sel;
 
     using Core = WarpCore<kE4M3>;
-    uint2* qs = q_stage(sm, w);
-    Core::stage_q(qs, a.q + ((size_t)r * a.Hq + (size_t)j * a.G) * kD, a.G, lane);
+    const CtaSmem<kE4M3> cs = CtaSmem<kE4M3>::carve(smem_raw, w);
+    WarpRing<kE4M3, kStages<kE4M3>()> rg;
+    rg.init(cs.ring, cs.masks);
+    Core::stage_q(cs.qs, a.q + ((size_t)r * a.Hq + (size_t)j * a.G) * kD, a.G, lane);
     Core wc;
     wc.reset();
     // half-tile h = block entries 2h, 2h+1 (8 tokens); lane t < 8 resolves token t
-    auto offsets = [&](int h, int64_t& ok, int64_t& o0, int64_t& o1) {
-        int64_t off = -1;
+    auto offset = [&](int h) -> int64_t {
         if (lane < kHalf) {
             const int t = prefill_token(sel_row, a.n_sel, own, p, 2 * h + (lane >> 2), lane & 3,
                                         flags);
             if (t >= 0)
-                off = token_row_offset(a.kv, a.bt, t, j, flags);
+                return token_row_offset(a.kv, a.bt, t, j, flags);
         }
-        ok = __shfl_sync(0xffffffffu, off, g);
-        o0 = __shfl_sync(0xffffffffu, off, 2 * q);
-        o1 = __shfl_sync(0xffffffffu, off, 2 * q + 1);
+        return -1;
     };
-    run_halves<kE4M3, kRing<kE4M3>()>(wc, qs, a.kv.k, a.kv.v, w, n_halves, kWarps, g < a.G,
-                                      a.scale_log2, lane, offsets);
-    cta_merge<kE4M3>(sm, wc, a.G, a.v_scale, out_rows, nullptr);
+    run_halves<kE4M3, kStages<kE4M3>()>(wc, rg, cs.qs, a.kv.k, a.kv.v, w, n_halves, kWarps,
+                                        g < a.G, a.scale_log2, lane, offset);
+    cta_merge<kE4M3>(*cs.merge, wc, a.G, a.v_scale, out_rows, nullptr);
     raise_flag(a.err, flags);
+}
+
+// Dynamic shared-memory opt-in, once per device and instantiation.
+template <bool kE4M3>
+static cudaError_t prefill_smem_attr()
+{
+    static std::atomic<int> done[kMaxDevices];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < kMaxDevices && done[dev].load(std::memory_order_acquire))
+        return cudaSuccess;
+    e = cudaFuncSetAttribute(sparse_prefill_kernel<kE4M3>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)SmemPlan<kE4M3>::kTailOff);
+    if (e == cudaSuccess && dev < kMaxDevices)
+        done[dev].store(1, std::memory_order_release);
+    return e;
 }
 
 cudaError_t launch_prefill(const PrefillArgs& a, bool e4m3, cudaStream_t s)
 {
+    cudaError_t e = e4m3 ? prefill_smem_attr<true>() : prefill_smem_attr<false>();
+    if (e != cudaSuccess)
+        return e;
     const dim3 grid(a.R, a.Hkv);
     if (e4m3)
-        sparse_prefill_kernel<true><<<grid, kThreads, 0, s>>>(a);
+        sparse_prefill_kernel<true><<<grid, kThreads, SmemPlan<true>::kTailOff, s>>>(a);
     else
-        sparse_prefill_kernel<false><<<grid, kThreads, 0, s>>>(a);
+        sparse_prefill_kernel<false><<<grid, kThreads, SmemPlan<false>::kTailOff, s>>>(a);
     return cudaGetLastError();
 }
 
