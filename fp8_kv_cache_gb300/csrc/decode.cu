@@ -78,7 +78,7 @@ __device__ void zero_rows(__half* rows, int G)
 }  // namespace
 
 template <bool kE4M3>
-__global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(DecodeArgs a)
+__global__ void __launch_bounds__(kThreads, kMinCtas<kE4M3>()) decode_split_kernel(DecodeArgs a)
 {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     const CtaSmem<kE4M3> cs = CtaSmem<kE4M3>::carve(smem_raw, threadIdx.x >> 5);
@@ -202,14 +202,17 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(DecodeArgs a)
 // head-dim values each): zero rows for empty sequences, nothing for segments
 // one split CTA covered, else the fixed-order LSE merge of the pieces
 //   M = max m_i,  O = sum_i 2^(m_i - M) O_i / sum_i 2^(m_i - M) l_i.
-// Launched as a programmatic dependent of the split kernel: it may start
-// early and waits on griddepcontrol.wait for the split kernel's results.
+// The pieces' (m, l) go through shared memory first so that every O load
+// can be in flight at once.  Launched as a programmatic dependent of the
+// split kernel: it may start early and waits on griddepcontrol.wait.
 __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeArgs a)
 {
+    __shared__ float w_s[kMergeThreads];
+    __shared__ float red_s[2];
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int h = blockIdx.x, b = blockIdx.y;
     const int j = h / a.G, hh = h - j * a.G;
-    const int d = 4 * threadIdx.x;
+    const int tid = threadIdx.x, d = 4 * tid;
     const int64_t T = a.hdr[0], C = a.hdr[1];
     const int64_t* P = a.hdr + 2;
     const int64_t nb = P[b + 1] - P[b];
@@ -226,27 +229,61 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeArgs 
     if (c_first == c_last)
         return;
     const int64_t k = (int64_t)b * a.Hkv + j;
-    // CTAs with an empty tile range (possible when C > T) wrote no slot.
-    auto empty = [&](int64_t c) { return c * T / C == (c + 1) * T / C; };
-    float M = -INFINITY;
-    for (int64_t c = c_first; c <= c_last; ++c)
-        if (!empty(c))
-            M = fmaxf(M, a.slots[(size_t)(c + k) * kSlotFloats + hh]);
+    const float* base = a.slots + (size_t)(c_first + k) * kSlotFloats;
     float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
-    float den = 0.f;
-    if (M != -INFINITY) {
-        for (int64_t c = c_first; c <= c_last; ++c) {
-            if (empty(c))
-                continue;
-            const float* sl = a.slots + (size_t)(c + k) * kSlotFloats;
-            const float e = ex2(sl[hh] - M);
-            den += e * sl[kGMax + hh];
-            const float4 o = *reinterpret_cast<const float4*>(sl + 2 * kGMax + hh * kD + d);
-            num.x += e * o.x;
-            num.y += e * o.y;
-            num.z += e * o.z;
-            num.w += e * o.w;
+    float den = 0.f, M_run = -INFINITY;
+    // pieces in chunks of kMergeThreads: thread i loads (m, l) of piece c0 + i
+    for (int64_t c0 = c_first; c0 <= c_last; c0 += kMergeThreads) {
+        const int np = (int)min((int64_t)kMergeThreads, c_last - c0 + 1);
+        float m_i = -INFINITY, l_i = 0.f;
+        if (tid < np) {
+            const int64_t c = c0 + tid;
+            // CTAs with an empty tile range (possible when C > T) wrote no slot.
+            if (c * T / C != (c + 1) * T / C) {
+                const float* sl = base + (size_t)(c - c_first) * kSlotFloats;
+                m_i = sl[hh];
+                l_i = sl[kGMax + hh];
+            }
         }
+        float mx = m_i;
+        for (int o = 16; o > 0; o >>= 1)
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if ((tid & 31) == 0)
+            red_s[tid >> 5] = mx;
+        __syncthreads();
+        const float M_new = fmaxf(M_run, fmaxf(red_s[0], red_s[1]));
+        __syncthreads();
+        if (M_new == -INFINITY)
+            continue;                        // nothing attended so far (CTA-uniform)
+        const float carry = (M_run == -INFINITY) ? 0.f : ex2(M_run - M_new);
+        num.x *= carry;
+        num.y *= carry;
+        num.z *= carry;
+        num.w *= carry;
+        den *= carry;
+        M_run = M_new;
+        const float wi = (m_i == -INFINITY) ? 0.f : ex2(m_i - M_new);
+        w_s[tid] = wi;
+        float part = wi * l_i;
+        for (int o = 16; o > 0; o >>= 1)
+            part += __shfl_xor_sync(0xffffffffu, part, o);
+        if ((tid & 31) == 0)
+            red_s[tid >> 5] = part;
+        __syncthreads();
+        den += red_s[0] + red_s[1];
+        const float* o_base = base + (size_t)(c0 - c_first) * kSlotFloats + 2 * kGMax + hh * kD + d;
+#pragma unroll 8
+        for (int i = 0; i < np; ++i) {
+            const float e = w_s[i];
+            if (e != 0.f) {
+                const float4 o = *reinterpret_cast<const float4*>(o_base + (size_t)i * kSlotFloats);
+                num.x += e * o.x;
+                num.y += e * o.y;
+                num.z += e * o.z;
+                num.w += e * o.w;
+            }
+        }
+        __syncthreads();                     // w_s and red_s are reused by the next chunk
     }
     const float sc = den > 0.f ? a.v_scale / den : 0.f;
     out2[0] = __floats2half2_rn(num.x * sc, num.y * sc);

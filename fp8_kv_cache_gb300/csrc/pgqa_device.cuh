@@ -235,7 +235,13 @@ struct WarpCore {
                          int lane)
     {
         const int q = lane & 3;
-        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+        // four independent accumulation chains over the 16 k-steps
+        float sc[4][4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                sc[c][e] = 0.f;
 #pragma unroll
         for (int s = 0; s < 16; ++s) {
             const uint2 a = qs[s * 32 + lane];
@@ -246,14 +252,13 @@ struct WarpCore {
                 b0 = word(t.k[s >> 1], 2 * (s & 1));
                 b1 = word(t.k[s >> 1], 2 * (s & 1) + 1);
             }
-            if (s & 1)
-                mma16816(sb, a.x, 0u, a.y, 0u, b0, b1);
-            else
-                mma16816(sa, a.x, 0u, a.y, 0u, b0, b1);
+            mma16816(sc[s & 3], a.x, 0u, a.y, 0u, b0, b1);
         }
         // scores of head g for tokens 2q, 2q+1
-        float x0 = (t.valid[0] && head_ok) ? (sa[0] + sb[0]) * scale_log2 : -INFINITY;
-        float x1 = (t.valid[1] && head_ok) ? (sa[1] + sb[1]) * scale_log2 : -INFINITY;
+        const float s0 = (sc[0][0] + sc[1][0]) + (sc[2][0] + sc[3][0]);
+        const float s1 = (sc[0][1] + sc[1][1]) + (sc[2][1] + sc[3][1]);
+        float x0 = (t.valid[0] && head_ok) ? s0 * scale_log2 : -INFINITY;
+        float x1 = (t.valid[1] && head_ok) ? s1 * scale_log2 : -INFINITY;
         float mx = fmaxf(x0, x1);
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
@@ -314,11 +319,21 @@ struct Stage {
 };
 
 // Ring depth (stages per warp): kNS - 1 half-tiles stay in flight while one
-// is read.  Chosen so that two CTAs of four warps fit on one SM.
+// is read.  With the CTAs per SM below, an SM keeps 96 KB (E4M3: 12 warps x
+// 2 x 4 KB) or 70 KB (FP16: 8 warps x 1 x 8.6 KB) of KV in flight, and the
+// shared memory of those CTAs fits in 228 KB.
 template <bool kE4M3>
 __host__ __device__ constexpr int kStages()
 {
-    return kE4M3 ? 4 : 2;
+    return kE4M3 ? 3 : 2;
+}
+
+// Resident CTAs per SM the attention kernels are compiled for (registers:
+// 65536 / (128 threads x CTAs)).
+template <bool kE4M3>
+__host__ __device__ constexpr int kMinCtas()
+{
+    return kE4M3 ? 3 : 2;
 }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p)

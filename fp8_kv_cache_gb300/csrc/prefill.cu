@@ -23,7 +23,7 @@
 namespace pgqa {
 
 template <bool kE4M3>
-__global__ void __launch_bounds__(kThreads, 2) sparse_prefill_kernel(PrefillArgs a)
+__global__ void __launch_bounds__(kThreads, kMinCtas<kE4M3>()) sparse_prefill_kernel(PrefillArgs a)
 {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     const int r = blockIdx.x, j = blockIdx.y;
