@@ -41,18 +41,18 @@ __device__ __forceinline__ int find_seq(const int64_t* P, int B, int Hkv, int64_
     return lo;
 }
 
-// The tiles [ta, te) of segment (b, j) processed by this CTA's warps (as
-// half-tiles of 8 tokens, round-robin), then merged into out_rows (final) or
-// slot (partial).
+// The tiles [ta, te) of segment (b, j) processed by this CTA's warps
+// (16-token tiles, round-robin), then merged into out_rows (final) or slot
+// (partial).  CTA-uniform: every thread of the CTA calls it.
 template <bool kE4M3>
 __device__ void run_piece(const DecodeArgs& a, const CtaSmem<kE4M3>& cs,
                           WarpRing<kE4M3, kStages<kE4M3>()>& rg, int b, int j, int L, int ta,
                           int te, __half* out_rows, float* slot, int& flags)
 {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const int g = lane >> 2;
     using Core = WarpCore<kE4M3>;
-    Core::stage_q(cs.qs, a.q + ((size_t)b * a.Hq + (size_t)j * a.G) * kD, a.G, lane);
+    Core::stage_q(cs.qs, a.q + ((size_t)b * a.Hq + (size_t)j * a.G) * kD, a.G, lane, w);
+    __syncthreads();
     Core wc;
     wc.reset();
     const int32_t* bt_row = a.bt + (int64_t)b * a.bt_stride;
@@ -64,8 +64,8 @@ __device__ void run_piece(const DecodeArgs& a, const CtaSmem<kE4M3>& cs,
         }
         return -1;
     };
-    run_halves<kE4M3, kStages<kE4M3>()>(wc, rg, cs.qs, a.kv.k, a.kv.v, 2 * ta + w, 2 * te, kWarps,
-                                        g < a.G, a.scale_log2, lane, offset);
+    run_tiles<kE4M3, kStages<kE4M3>()>(wc, rg, cs.qs, a.kv.k, a.kv.v, ta + w, te, kWarps, a.G,
+                                       a.scale_log2, lane, offset);
     cta_merge<kE4M3>(*cs.merge, wc, a.G, a.v_scale, out_rows, slot);
 }
 

@@ -157,184 +157,7 @@ __device__ __forceinline__ int prefill_token(const int32_t* sel_row, int n_sel, 
     return -1;
 }
 
-// ------------------------------------------------------------------ warp core
-
-// D(16x8, f32) += A(16x8, f16, row) * B(8x8, f16, col).
-__device__ __forceinline__ void mma16808(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t b0)
-{
-    asm("mma.sync.aligned.m16n8k8.row.col.f32.f16.f16.f32 "
-        "{%0,%1,%2,%3}, {%4,%5}, {%6}, {%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a0), "r"(a1), "r"(b0));
-}
-
-// Raw K/V registers of one half-tile (8 tokens) as lane (g, q) holds them:
-// the K row of token g and the V rows of tokens 2q and 2q+1.
-template <bool kE4M3>
-struct HalfTile {
-    static constexpr int kKCh = kE4M3 ? 4 : 8;   // 16-byte chunks of the K row
-    static constexpr int kVCh = kE4M3 ? 2 : 4;   // 16-byte chunks of each V row
-    uint4 k[kKCh];
-    uint4 v[2][kVCh];
-    bool valid[2];                               // tokens 2q, 2q+1 attended
-};
-
-// Register-resident attention state of one warp for one (sequence or row,
-// KV head): O^T accumulators, the softmax denominators and the running max of
-// head g (= lane / 4).  The Q fragments live in shared memory (qs), laid out
-// [k-step][lane] as uint2 so each lane reads 8 contiguous bytes.
-template <bool kE4M3>
-struct WarpCore {
-    float acc[17][4];     // [0..15]: O^T fragments, [16]: denominators
-    float m;              // running max of head g, log2 domain
-
-    // Head-dim index of element n (0..63) of the K-row chunks lane q holds
-    // (chunk c = q + 4i is 16 bytes at byte offset 16c of the row).
-    __device__ static int k_dim(int q, int n)
-    {
-        return kE4M3 ? 16 * (q + 4 * (n >> 4)) + (n & 15) : 8 * (q + 4 * (n >> 3)) + (n & 7);
-    }
-    // Head-dim index of output slot n (0..31) of lane group g (V chunk i is
-    // 16 bytes at byte offset 16g + 128i of the row).
-    __device__ static int v_dim(int g, int n)
-    {
-        return kE4M3 ? 16 * g + 128 * (n >> 4) + (n & 15) : 8 * g + 64 * (n >> 3) + (n & 7);
-    }
-
-    // Writes this lane's Q fragments (heads g < G of the group, binary16
-    // [G][256] rows at qg) into qs[16][32] (uint2), then syncs the warp.
-    __device__ static void stage_q(uint2* qs, const __half* qg, int G, int lane)
-    {
-        const int g = lane >> 2, q = lane & 3;
-        const uint32_t* row = reinterpret_cast<const uint32_t*>(qg + (size_t)g * kD);
-#pragma unroll
-        for (int s = 0; s < 16; ++s) {
-            uint2 f = make_uint2(0u, 0u);
-            if (g < G) {
-                f.x = __ldg(row + (k_dim(q, 4 * s) >> 1));
-                f.y = __ldg(row + (k_dim(q, 4 * s + 2) >> 1));
-            }
-            qs[s * 32 + lane] = f;
-        }
-        __syncwarp();
-    }
-
-    __device__ void reset()
-    {
-#pragma unroll
-        for (int i = 0; i < 17; ++i)
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-                acc[i][c] = 0.f;
-        m = -INFINITY;
-    }
-
-    // One half-tile of 8 tokens: S = Q K^T (m16n8k16, rows = heads), online
-    // softmax of head g, then O^T += V^T P^T and l += 1^T P^T (m16n8k8).
-    __device__ void step(const HalfTile<kE4M3>& t, const uint2* qs, bool head_ok, float scale_log2,
-                         int lane)
-    {
-        const int q = lane & 3;
-        // four independent accumulation chains over the 16 k-steps
-        float sc[4][4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                sc[c][e] = 0.f;
-#pragma unroll
-        for (int s = 0; s < 16; ++s) {
-            const uint2 a = qs[s * 32 + lane];
-            uint32_t b0, b1;
-            if (kE4M3) {
-                e4m3x4_to_f16x2x2(word(t.k[s >> 2], s & 3), b0, b1);
-            } else {
-                b0 = word(t.k[s >> 1], 2 * (s & 1));
-                b1 = word(t.k[s >> 1], 2 * (s & 1) + 1);
-            }
-            mma16816(sc[s & 3], a.x, 0u, a.y, 0u, b0, b1);
-        }
-        // scores of head g for tokens 2q, 2q+1
-        const float s0 = (sc[0][0] + sc[1][0]) + (sc[2][0] + sc[3][0]);
-        const float s1 = (sc[0][1] + sc[1][1]) + (sc[2][1] + sc[3][1]);
-        float x0 = (t.valid[0] && head_ok) ? s0 * scale_log2 : -INFINITY;
-        float x1 = (t.valid[1] && head_ok) ? s1 * scale_log2 : -INFINITY;
-        float mx = fmaxf(x0, x1);
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const float m_new = fmaxf(m, mx);
-        float alpha = 1.f, p0 = 0.f, p1 = 0.f;
-        if (m_new != -INFINITY) {
-            alpha = ex2(m - m_new);
-            p0 = ex2(x0 - m_new);
-            p1 = ex2(x1 - m_new);
-        }
-        m = m_new;
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
-            const float a_lo = __shfl_sync(0xffffffffu, alpha, 8 * q);
-            const float a_hi = __shfl_sync(0xffffffffu, alpha, 8 * q + 4);
-#pragma unroll
-            for (int i = 0; i < 17; ++i) {
-                acc[i][0] *= a_lo;
-                acc[i][2] *= a_lo;
-                acc[i][1] *= a_hi;
-                acc[i][3] *= a_hi;
-            }
-        }
-        const uint32_t pb = pack_half2(p0, p1);
-#pragma unroll
-        for (int mt = 0; mt < 16; ++mt) {
-            uint32_t a0, a1;
-            if (kE4M3) {
-                const int i = mt >> 3, w = (mt & 7) >> 1;
-                const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
-                e4m3x4_to_f16x2x2(__byte_perm(word(t.v[0][i], w), word(t.v[1][i], w), sel), a0, a1);
-            } else {
-                const int i = mt >> 2, w = mt & 3;
-                a0 = __byte_perm(word(t.v[0][i], w), word(t.v[1][i], w), 0x5410u);
-                a1 = __byte_perm(word(t.v[0][i], w), word(t.v[1][i], w), 0x7632u);
-            }
-            mma16808(acc[mt], a0, a1, pb);
-        }
-        const uint32_t one2 = 0x3C003C00u;   // half2(1, 1)
-        mma16808(acc[16], one2, one2, pb);
-    }
-};
-
 // ------------------------------------------------------------------ async ring
-
-// One stage of a warp's shared-memory ring holds one half-tile: the K rows of
-// its 8 tokens, then their V rows.  Row strides are padded so that the
-// fragment reads below are free of bank conflicts: a K row is read by lanes
-// (g, q) as chunks q + 4i (8 rows x 4 chunks per quarter-warp phase -> the
-// stride must be 64 mod 128 bytes); a V row pair 2q, 2q+1 is read at chunk
-// g + 8i (stride 16 mod 64 bytes).
-template <bool kE4M3>
-struct Stage {
-    static constexpr int kRowBytes = kE4M3 ? 256 : 512;
-    static constexpr int kKStride = kRowBytes + 64;
-    static constexpr int kVStride = kRowBytes + 16;
-    static constexpr int kKBytes = kHalf * kKStride;
-    static constexpr int kBytes = kHalf * (kKStride + kVStride);
-};
-
-// Ring depth (stages per warp): kNS - 1 half-tiles stay in flight while one
-// is read.  With the CTAs per SM below, an SM keeps 96 KB (E4M3: 12 warps x
-// 2 x 4 KB) or 70 KB (FP16: 8 warps x 1 x 8.6 KB) of KV in flight, and the
-// shared memory of those CTAs fits in 228 KB.
-template <bool kE4M3>
-__host__ __device__ constexpr int kStages()
-{
-    return kE4M3 ? 3 : 2;
-}
-
-// Resident CTAs per SM the attention kernels are compiled for (registers:
-// 65536 / (128 threads x CTAs)).
-template <bool kE4M3>
-__host__ __device__ constexpr int kMinCtas()
-{
-    return kE4M3 ? 3 : 2;
-}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p)
 {
@@ -366,6 +189,42 @@ __device__ __forceinline__ void cp_async_wait()
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// One stage of a warp's shared-memory ring holds one half-tile: the K rows of
+// its 8 tokens, then their V rows, unpadded.  16-byte chunks are placed with
+// an XOR swizzle so that the fragment reads of the tile step are free of bank
+// conflicts: chunk c of K row t sits at chunk c ^ 4(t & 1) (a quarter-warp
+// reads chunks q + 4i of rows g, g+1), chunk c of V row t at c ^ 2((t >> 1) & 3)
+// (a quarter-warp reads chunk g of rows 2q + u for four q).
+template <bool kE4M3>
+struct Stage {
+    static constexpr int kRowBytes = kE4M3 ? 256 : 512;
+    static constexpr int kKBytes = kHalf * kRowBytes;
+    static constexpr int kBytes = 2 * kKBytes;
+    __device__ static uint32_t k_off(int t, int c) { return t * kRowBytes + ((16 * c) ^ (64 * (t & 1))); }
+    __device__ static uint32_t v_off(int t, int c)
+    {
+        return kKBytes + t * kRowBytes + ((16 * c) ^ (32 * ((t >> 1) & 3)));
+    }
+};
+
+// Ring depth in half-tiles per warp.  A 16-token tile consumes two stages, so
+// kNS - 2 half-tiles stay in flight while a tile is computed: E4M3 keeps
+// 2 x 4 KB per warp (12 warps per SM: 96 KB in flight), FP16 1 x 8 KB (8 warps
+// per SM: 64 KB in flight), and the CTAs' shared memory fits in 228 KB.
+template <bool kE4M3>
+__host__ __device__ constexpr int kStages()
+{
+    return kE4M3 ? 4 : 3;
+}
+
+// Resident CTAs per SM the attention kernels are compiled for (registers:
+// 65536 / (128 threads x CTAs)).
+template <bool kE4M3>
+__host__ __device__ constexpr int kMinCtas()
+{
+    return kE4M3 ? 3 : 2;
+}
+
 // A warp's private ring of kNS stages filled by 16-byte asynchronous copies
 // (global -> shared, bypassing L1).  Each fill is one commit group per lane;
 // a stage is ready once every lane's group for it has completed and the warp
@@ -374,7 +233,7 @@ __device__ __forceinline__ void cp_async_wait()
 template <bool kE4M3, int kNS>
 struct WarpRing {
     uint32_t ring;        // shared address of stage 0
-    uint32_t* masks;      // kNS words: bit t = token t of the stage is valid
+    uint32_t* masks;      // kNS words: bit t = token t of the stage is attended
 
     __device__ void init(unsigned char* ring_ptr, uint32_t* mask_ptr)
     {
@@ -382,11 +241,16 @@ struct WarpRing {
         masks = mask_ptr;
     }
 
+    __device__ uint32_t addr(int s) const
+    {
+        return ring + s * Stage<kE4M3>::kBytes;
+    }
+
     // Starts filling stage s and commits one group.  Lane t < 8 passes the
     // byte offset of token t's rows (K and V share it), or < 0 when the token
-    // is not attended.  Chunk c of a row is copied by lane c (FP16 rows are
-    // 32 chunks) or lane c + 16 * (row parity) (E4M3 rows are 16 chunks), so
-    // every copy instruction reads whole 512-byte row pieces.
+    // is not attended.  Each copy instruction moves whole 512-byte pieces of
+    // rows: FP16 row chunks go to lanes 0..31, E4M3 rows are 16 chunks, so
+    // lanes 0..15 take one row and lanes 16..31 the next.
     __device__ void fill(int s, int64_t off, const unsigned char* kb, const unsigned char* vb,
                          int lane)
     {
@@ -394,41 +258,39 @@ struct WarpRing {
         const uint32_t mask = __ballot_sync(0xffffffffu, lane < kHalf && off >= 0) & 0xFFu;
         if (lane == 0)
             masks[s] = mask;
-        const uint32_t base = ring + s * St::kBytes;
+        const uint32_t base = addr(s);
         if (kE4M3) {
-            // instruction k: token 2(k % 4) + lane / 16, chunk lane % 16, K for k < 4
-            const int half = lane >> 4, c = lane & 15;
+            const int c = lane & 15;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const int t = 2 * k + half;
+                const int t = 2 * k + (lane >> 4);
                 const int64_t o = __shfl_sync(0xffffffffu, off, t);
                 if ((mask >> t) & 1u) {
-                    cp_async16(base + t * St::kKStride + 16 * c, kb + o + 16 * c);
-                    cp_async16(base + St::kKBytes + t * St::kVStride + 16 * c, vb + o + 16 * c);
+                    cp_async16(base + St::k_off(t, c), kb + o + 16 * c);
+                    cp_async16(base + St::v_off(t, c), vb + o + 16 * c);
                 }
             }
         } else {
-            // instruction k: token k, chunk lane
 #pragma unroll
             for (int t = 0; t < kHalf; ++t) {
                 const int64_t o = __shfl_sync(0xffffffffu, off, t);
                 if ((mask >> t) & 1u) {
-                    cp_async16(base + t * St::kKStride + 16 * lane, kb + o + 16 * lane);
-                    cp_async16(base + St::kKBytes + t * St::kVStride + 16 * lane, vb + o + 16 * lane);
+                    cp_async16(base + St::k_off(t, lane), kb + o + 16 * lane);
+                    cp_async16(base + St::v_off(t, lane), vb + o + 16 * lane);
                 }
             }
         }
         cp_async_commit();
     }
 
-    // Commits an empty group (keeps one group per ring slot).
+    // Commits an empty group (one group per ring slot keeps the counts fixed).
     __device__ void skip() const
     {
         cp_async_commit();
     }
 
-    // The oldest of the kNS - 1 committed fills is complete for every lane
-    // (at most kNS - 2 groups may still be pending).
+    // With kNS fills committed ahead of the current tile, the tile's two
+    // stages are complete once at most kNS - 2 groups remain pending.
     __device__ void wait() const
     {
         static_assert(kNS >= 2, "the ring needs at least two stages");
@@ -441,78 +303,229 @@ struct WarpRing {
         asm volatile("cp.async.wait_all;" ::: "memory");
         __syncwarp();
     }
+};
 
-    // The fragments lane (g, q) needs from stage s: K row g, V rows 2q, 2q+1
-    // (zeros for tokens that are not attended).
-    __device__ void read(int s, HalfTile<kE4M3>& t, int g, int q) const
+// ------------------------------------------------------------------ warp core
+
+// Register-resident attention state of one warp for one (sequence or row,
+// KV head): O^T accumulators, the softmax denominators and the running maxima
+// of heads 2q and 2q+1 (q = lane & 3).  The Q fragments live in shared
+// memory (qs, [k-step][lane] as uint2), shared by the CTA's warps.
+//
+// Per 16-token tile (two ring stages):
+//   S^T = K Q^T   m16n8k16, rows = the 16 tokens, columns = 8 (padded) heads,
+//                 K straight from the stage (E4M3 -> f16 in registers);
+//   softmax       per head over the tile's 16 tokens (3 shuffles per head);
+//   P^T -> P      two movmatrix transposes turn the probabilities of the C
+//                 fragment into the B fragment of the next product;
+//   O^T += V^T P^T and l += 1^T P^T   m16n8k16 over the 16 tokens.
+template <bool kE4M3>
+struct WarpCore {
+    static constexpr int kKCh = kE4M3 ? 4 : 8;   // 16-byte chunks of a K row per lane
+    static constexpr int kVCh = kE4M3 ? 2 : 4;   // 16-byte chunks of a V row per lane
+
+    float acc[17][4];     // [0..15]: O^T fragments, [16]: denominators
+    float m0, m1;         // running max of heads 2q, 2q+1, log2 domain
+
+    // Head-dim index of element n (0..63) of the K-row chunks lane q holds
+    // (logical chunk c = q + 4i is the 16 bytes at byte 16c of the row).
+    __device__ static int k_dim(int q, int n)
+    {
+        return kE4M3 ? 16 * (q + 4 * (n >> 4)) + (n & 15) : 8 * (q + 4 * (n >> 3)) + (n & 7);
+    }
+    // Head-dim index of output slot n (0..31) of lane group g (logical V
+    // chunk g + 8i).
+    __device__ static int v_dim(int g, int n)
+    {
+        return kE4M3 ? 16 * g + 128 * (n >> 4) + (n & 15) : 8 * g + 64 * (n >> 3) + (n & 7);
+    }
+
+    // The CTA's warps write the Q fragments of heads g < G (binary16 [G][256]
+    // rows at qg) into qs[16][32] (uint2), four k-steps each; the caller
+    // synchronises the CTA before use.
+    __device__ static void stage_q(uint2* qs, const __half* qg, int G, int lane, int w)
+    {
+        const int g = lane >> 2, q = lane & 3;
+        const uint32_t* row = reinterpret_cast<const uint32_t*>(qg + (size_t)g * kD);
+#pragma unroll
+        for (int k = 0; k < 16 / kWarps; ++k) {
+            const int s = w * (16 / kWarps) + k;
+            uint2 f = make_uint2(0u, 0u);
+            if (g < G) {
+                f.x = __ldg(row + (k_dim(q, 4 * s) >> 1));
+                f.y = __ldg(row + (k_dim(q, 4 * s + 2) >> 1));
+            }
+            qs[s * 32 + lane] = f;
+        }
+    }
+
+    __device__ void reset()
+    {
+#pragma unroll
+        for (int i = 0; i < 17; ++i)
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                acc[i][c] = 0.f;
+        m0 = m1 = -INFINITY;
+    }
+
+    // One 16-token tile whose first 8 tokens are in stage st0 and last 8 in
+    // st1; bit t of mask says whether token t is attended.
+    __device__ void tile(uint32_t st0, uint32_t st1, uint32_t mask, const uint2* qs, int G,
+                         float scale_log2, int lane)
     {
         using St = Stage<kE4M3>;
-        const uint32_t mask = masks[s];
-        const uint32_t base = ring + s * St::kBytes;
-        const bool kv = (mask >> g) & 1u;
+        const int g = lane >> 2, q = lane & 3;
+        const uint4 zero = make_uint4(0, 0, 0, 0);
+        // ---- S^T = K Q^T over the 16 k-steps, four accumulation chains
+        float sc[4][4];
 #pragma unroll
-        for (int i = 0; i < HalfTile<kE4M3>::kKCh; ++i)
-            t.k[i] = kv ? lds128(base + g * St::kKStride + 16 * (q + 4 * i)) : make_uint4(0, 0, 0, 0);
+        for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const int row = 2 * q + u;
-            const bool vv = (mask >> row) & 1u;
-            t.valid[u] = vv;
+            for (int e = 0; e < 4; ++e)
+                sc[c][e] = 0.f;
+        const bool kv0 = (mask >> g) & 1u, kv1 = (mask >> (g + 8)) & 1u;
 #pragma unroll
-            for (int i = 0; i < HalfTile<kE4M3>::kVCh; ++i)
-                t.v[u][i] = vv ? lds128(base + St::kKBytes + row * St::kVStride + 16 * g + 128 * i)
-                               : make_uint4(0, 0, 0, 0);
+        for (int i = 0; i < kKCh; ++i) {
+            const uint4 k0 = kv0 ? lds128(st0 + St::k_off(g, q + 4 * i)) : zero;   // token g
+            const uint4 k1 = kv1 ? lds128(st1 + St::k_off(g, q + 4 * i)) : zero;   // token g + 8
+#pragma unroll
+            for (int w = 0; w < (kE4M3 ? 4 : 2); ++w) {
+                const int s = kE4M3 ? 4 * i + w : 2 * i + w;
+                const uint2 b = qs[s * 32 + lane];
+                uint32_t a0, a1, a2, a3;
+                if (kE4M3) {
+                    e4m3x4_to_f16x2x2(word(k0, w), a0, a2);
+                    e4m3x4_to_f16x2x2(word(k1, w), a1, a3);
+                } else {
+                    a0 = word(k0, 2 * w);
+                    a2 = word(k0, 2 * w + 1);
+                    a1 = word(k1, 2 * w);
+                    a3 = word(k1, 2 * w + 1);
+                }
+                mma16816(sc[s & 3], a0, a1, a2, a3, b.x, b.y);
+            }
         }
+        // ---- online softmax: lane holds tokens g, g+8 of heads 2q, 2q+1
+        const bool h0 = 2 * q < G, h1 = 2 * q + 1 < G;
+        float x[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            x[e] = (sc[0][e] + sc[1][e]) + (sc[2][e] + sc[3][e]);
+        x[0] = (kv0 && h0) ? x[0] * scale_log2 : -INFINITY;   // token g,     head 2q
+        x[1] = (kv0 && h1) ? x[1] * scale_log2 : -INFINITY;   // token g,     head 2q+1
+        x[2] = (kv1 && h0) ? x[2] * scale_log2 : -INFINITY;   // token g + 8, head 2q
+        x[3] = (kv1 && h1) ? x[3] * scale_log2 : -INFINITY;   // token g + 8, head 2q+1
+        float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+        }
+        const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+        const float al0 = n0 == -INFINITY ? 1.f : ex2(m0 - n0);
+        const float al1 = n1 == -INFINITY ? 1.f : ex2(m1 - n1);
+        float p[4];
+        p[0] = n0 == -INFINITY ? 0.f : ex2(x[0] - n0);
+        p[2] = n0 == -INFINITY ? 0.f : ex2(x[2] - n0);
+        p[1] = n1 == -INFINITY ? 0.f : ex2(x[1] - n1);
+        p[3] = n1 == -INFINITY ? 0.f : ex2(x[3] - n1);
+        m0 = n0;
+        m1 = n1;
+        if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+            for (int i = 0; i < 17; ++i) {
+                acc[i][0] *= al0;
+                acc[i][2] *= al0;
+                acc[i][1] *= al1;
+                acc[i][3] *= al1;
+            }
+        }
+        // ---- P fragments: transpose the two 8x8 blocks [token][head] -> [head][token]
+        uint32_t pb0, pb1;
+        asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(pb0) : "r"(pack_half2(p[0], p[1])));
+        asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(pb1) : "r"(pack_half2(p[2], p[3])));
+        // ---- O^T += V^T P^T: V rows 2q, 2q+1 (stage 0) and 2q+8, 2q+9 (stage 1)
+        const bool v0 = (mask >> (2 * q)) & 1u, v1 = (mask >> (2 * q + 1)) & 1u;
+        const bool v2 = (mask >> (2 * q + 8)) & 1u, v3 = (mask >> (2 * q + 9)) & 1u;
+#pragma unroll
+        for (int i = 0; i < kVCh; ++i) {
+            const int c = g + 8 * i;
+            const uint4 r0 = v0 ? lds128(st0 + St::v_off(2 * q, c)) : zero;
+            const uint4 r1 = v1 ? lds128(st0 + St::v_off(2 * q + 1, c)) : zero;
+            const uint4 r2 = v2 ? lds128(st1 + St::v_off(2 * q, c)) : zero;
+            const uint4 r3 = v3 ? lds128(st1 + St::v_off(2 * q + 1, c)) : zero;
+#pragma unroll
+            for (int j = 0; j < (kE4M3 ? 8 : 4); ++j) {
+                const int mt = (kE4M3 ? 8 : 4) * i + j;
+                uint32_t a0, a1, a2, a3;
+                if (kE4M3) {
+                    const int w = j >> 1;
+                    const uint32_t sel = (j & 1) ? 0x7362u : 0x5140u;
+                    e4m3x4_to_f16x2x2(__byte_perm(word(r0, w), word(r1, w), sel), a0, a1);
+                    e4m3x4_to_f16x2x2(__byte_perm(word(r2, w), word(r3, w), sel), a2, a3);
+                } else {
+                    a0 = __byte_perm(word(r0, j), word(r1, j), 0x5410u);
+                    a1 = __byte_perm(word(r0, j), word(r1, j), 0x7632u);
+                    a2 = __byte_perm(word(r2, j), word(r3, j), 0x5410u);
+                    a3 = __byte_perm(word(r2, j), word(r3, j), 0x7632u);
+                }
+                mma16816(acc[mt], a0, a1, a2, a3, pb0, pb1);
+            }
+        }
+        const uint32_t one2 = 0x3C003C00u;   // half2(1, 1)
+        mma16816(acc[16], one2, one2, one2, one2, pb0, pb1);
     }
 };
 
-// Runs a warp over half-tiles h = first, first + stride, ... < end through
-// its ring: kNS - 1 fills in flight; per half-tile: wait for the oldest fill,
-// read its fragments, refill that stage kNS - 1 half-tiles ahead, compute.
-// offset(h) returns, on lanes t < 8, the byte offset of token t of half-tile h
-// (or -1), and -1 on the other lanes.
+// Runs a warp over 16-token tiles k = first, first + stride, ... < end.  Tile
+// k is half-tiles 2k and 2k+1; offset(h) returns, on lanes t < 8, the byte
+// offset of token t of half-tile h (or -1), and -1 on the other lanes.  The
+// ring keeps kNS half-tiles committed ahead of the tile being computed.
 template <bool kE4M3, int kNS, class Offset>
-__device__ __forceinline__ void run_halves(WarpCore<kE4M3>& wc, WarpRing<kE4M3, kNS>& rg,
-                                           const uint2* qs, const unsigned char* kb,
-                                           const unsigned char* vb, int first, int end, int stride,
-                                           bool head_ok, float scale_log2, int lane, Offset offset)
+__device__ __forceinline__ void run_tiles(WarpCore<kE4M3>& wc, WarpRing<kE4M3, kNS>& rg,
+                                          const uint2* qs, const unsigned char* kb,
+                                          const unsigned char* vb, int first, int end, int stride,
+                                          int G, float scale_log2, int lane, Offset offset)
 {
-    const int g = lane >> 2, q = lane & 3;
     const int n = end > first ? (end - first + stride - 1) / stride : 0;
     if (n == 0)
         return;
-    for (int i = 0; i < kNS - 1; ++i) {
-        if (i < n)
-            rg.fill(i, offset(first + i * stride), kb, vb, lane);
+    const int H = 2 * n;                        // half-tiles of this warp, in order
+    auto half = [&](int j) { return 2 * (first + (j >> 1) * stride) + (j & 1); };
+    for (int j = 0; j < kNS; ++j) {
+        if (j < H)
+            rg.fill(j, offset(half(j)), kb, vb, lane);
         else
             rg.skip();
     }
-    for (int i = 0; i < n; ++i) {
-        const int s = i % kNS;
-        HalfTile<kE4M3> t;
+    for (int k = 0; k < n; ++k) {
+        const int s0 = (2 * k) % kNS, s1 = (2 * k + 1) % kNS;
         rg.wait();
-        rg.read(s, t, g, q);
+        const uint32_t mask = rg.masks[s0] | (rg.masks[s1] << 8);
+        wc.tile(rg.addr(s0), rg.addr(s1), mask, qs, G, scale_log2, lane);
         __syncwarp();
-        const int nf = i + kNS - 1;
-        if (nf < n)
-            rg.fill(nf % kNS, offset(first + nf * stride), kb, vb, lane);
-        else
-            rg.skip();
-        wc.step(t, qs, head_ok, scale_log2, lane);
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int j = 2 * k + kNS + u;
+            if (j < H)
+                rg.fill(j % kNS, offset(half(j)), kb, vb, lane);
+            else
+                rg.skip();
+        }
     }
     rg.drain();
 }
 
 // Shared-memory carve-up of a CTA of the attention kernels:
-//   [Q fragments of 4 warps][rings of 4 warps (the merge buffer aliases them)]
+//   [Q fragments (4 KB, shared)][rings of 4 warps (the merge buffer aliases them)]
 //   [stage masks][kernel-specific tail]
 template <bool kE4M3>
 struct SmemPlan {
     static constexpr int kNS = kStages<kE4M3>();
-    static constexpr size_t kQBytes = (size_t)kWarps * 16 * 32 * sizeof(uint2);
+    static constexpr size_t kQBytes = (size_t)16 * 32 * sizeof(uint2);
     static constexpr size_t kRingBytes = (size_t)kWarps * kNS * Stage<kE4M3>::kBytes;
-    static constexpr size_t kRingOrMerge = kRingBytes;   // asserted >= sizeof(MergeSmem) below
-    static constexpr size_t kMaskOff = kQBytes + kRingOrMerge;
+    static constexpr size_t kMaskOff = kQBytes + kRingBytes;
     static constexpr size_t kTailOff = (kMaskOff + (size_t)kWarps * kNS * 4 + 15) & ~(size_t)15;
 };
 
@@ -530,7 +543,7 @@ struct MergeSmem {
 // The pieces of a CTA's shared memory for one attention kernel instance.
 template <bool kE4M3>
 struct CtaSmem {
-    uint2* qs;            // this warp's Q fragments
+    uint2* qs;            // the CTA's Q fragments
     MergeSmem* merge;     // aliases the rings; used only after every ring is drained
     unsigned char* ring;  // this warp's ring
     uint32_t* masks;      // this warp's stage masks
@@ -541,7 +554,7 @@ struct CtaSmem {
         using Pl = SmemPlan<kE4M3>;
         static_assert(Pl::kRingBytes >= sizeof(MergeSmem), "merge buffer must fit in the rings");
         CtaSmem c;
-        c.qs = reinterpret_cast<uint2*>(base) + w * 16 * 32;
+        c.qs = reinterpret_cast<uint2*>(base);
         c.merge = reinterpret_cast<MergeSmem*>(base + Pl::kQBytes);
         c.ring = base + Pl::kQBytes + (size_t)w * Pl::kNS * Stage<kE4M3>::kBytes;
         c.masks = reinterpret_cast<uint32_t*>(base + Pl::kMaskOff) + w * Pl::kNS;
@@ -557,9 +570,9 @@ __device__ void cta_merge(MergeSmem& sm, const WarpCore<kE4M3>& wc, int G, float
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const int g = lane >> 2, q = lane & 3;
     __syncthreads();   // previous use of sm finished
-    if (q == 0)
-        sm.m[w][g] = wc.m;
     if (g == 0) {
+        sm.m[w][2 * q] = wc.m0;
+        sm.m[w][2 * q + 1] = wc.m1;
         sm.l[w][2 * q] = wc.acc[16][0];
         sm.l[w][2 * q + 1] = wc.acc[16][1];
     }

@@ -9,10 +9,11 @@
 // plain strides here.
 //
 // Design (ours): one CTA per (query row, KV head).  Its four warps take the
-// row's half-tiles (two block entries = 8 tokens each) round-robin; lane t of
-// 0..7 resolves token t (selected block id -> token -> page -> row address)
-// and the warp copies the K and V rows into its shared-memory ring with
-// 16-byte asynchronous copies, so the gather runs through the same tensor-core
+// row's 16-token tiles (four block entries each) round-robin; for each half
+// of a tile, lane t of 0..7 resolves token t (selected block id -> token ->
+// page -> row address) and the warp copies the K and V rows into its
+// shared-memory ring with 16-byte asynchronous copies, so the gather runs
+// through the same tensor-core
 // pipeline as decode; the warps then merge through shared memory and the CTA
 // writes the row's FP16 outputs.  No table of virtual pages is built: the
 // four-token block addresses are computed inline.
@@ -28,7 +29,6 @@ __global__ void __launch_bounds__(kThreads, kMinCtas<kE4M3>()) sparse_prefill_ke
     extern __shared__ __align__(128) unsigned char smem_raw[];
     const int r = blockIdx.x, j = blockIdx.y;
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const int g = lane >> 2;
     int flags = 0;
     __half* out_rows = a.out + ((size_t)r * a.Hq + (size_t)j * a.G) * kD;
 
@@ -46,14 +46,15 @@ __global__ void __launch_bounds__(kThreads, kMinCtas<kE4M3>()) sparse_prefill_ke
             flags |= PAGED_GQA_FLAG_QPOS_CLAMPED;
     }
     const int own = p >> 2;
-    const int n_halves = (a.n_sel + 1 + 1) / 2;  // selected entries + the tail entry, 2 per half
+    const int n_tiles = (a.n_sel + 1 + 3) / 4;   // selected entries + the tail entry, 4 per tile
     const int32_t* sel_row = a.sel + (size_t)r * a.n_sel;
 
     using Core = WarpCore<kE4M3>;
     const CtaSmem<kE4M3> cs = CtaSmem<kE4M3>::carve(smem_raw, w);
     WarpRing<kE4M3, kStages<kE4M3>()> rg;
     rg.init(cs.ring, cs.masks);
-    Core::stage_q(cs.qs, a.q + ((size_t)r * a.Hq + (size_t)j * a.G) * kD, a.G, lane);
+    Core::stage_q(cs.qs, a.q + ((size_t)r * a.Hq + (size_t)j * a.G) * kD, a.G, lane, w);
+    __syncthreads();
     Core wc;
     wc.reset();
     // half-tile h = block entries 2h, 2h+1 (8 tokens); lane t < 8 resolves token t
@@ -66,8 +67,8 @@ __global__ void __launch_bounds__(kThreads, kMinCtas<kE4M3>()) sparse_prefill_ke
         }
         return -1;
     };
-    run_halves<kE4M3, kStages<kE4M3>()>(wc, rg, cs.qs, a.kv.k, a.kv.v, w, n_halves, kWarps,
-                                        g < a.G, a.scale_log2, lane, offset);
+    run_tiles<kE4M3, kStages<kE4M3>()>(wc, rg, cs.qs, a.kv.k, a.kv.v, w, n_tiles, kWarps, a.G,
+                                       a.scale_log2, lane, offset);
     cta_merge<kE4M3>(*cs.merge, wc, a.G, a.v_scale, out_rows, nullptr);
     raise_flag(a.err, flags);
 }
