@@ -18,8 +18,9 @@
  * ---------------------------------------
  *  * Pointers named as device data point to memory on the current CUDA
  *    device, owned by the caller.  The library never allocates device or host
- *    memory, never frees caller memory and holds no state between calls, so
- *    concurrent calls from several host threads are safe.
+ *    memory and never frees caller memory.  Between calls it keeps only a
+ *    per-device cache of the SM count and kernel occupancy, so concurrent
+ *    calls from several host threads are safe.
  *  * Every call is asynchronous on `stream` (a cudaStream_t; NULL means the
  *    legacy default stream) and never synchronises the host, so calls can be
  *    captured into CUDA graphs.
