@@ -2,10 +2,11 @@
 // of the attention kernels, so tests can compare them bit for bit.
 //
 // They call the very device functions the attention kernels use:
-// token_row_offset (block table -> page -> row address), prefill_token
-// (selected block entry -> token, "[Kernel][SM70] Accelerate Qwen3.8 QSA
-// paged prefill", Changes), ldg_stream and the E4M3 converter e4m3x4_to_f16x2x2
-// ("[Kernel][SM70] Scale NVFP4 E4M3 decode batches", Purpose).
+// page_and_slot / table_page / row_offset (block table -> page -> row
+// address), prefill_entry / prefill_lane_live (selected block entry -> tokens,
+// "[Kernel][SM70] Accelerate Qwen3.8 QSA paged prefill", Changes), and the
+// E4M3 converter e4m3x4_to_f16x2x2 ("[Kernel][SM70] Scale NVFP4 E4M3 decode
+// batches", Purpose).
 #include "pgqa_internal.h"
 
 namespace pgqa {
@@ -78,9 +79,11 @@ __global__ void __launch_bounds__(128) prefill_tokens_kernel(KVGeom g, const int
         int t = -1;
         if (p >= 0 && kv_len > 0) {
             const int pc = p >= kv_len ? kv_len - 1 : p;
-            t = prefill_token(sel + (int64_t)r * n_sel, n_sel, pc >> 2, pc, s >> 2, s & 3, flags);
-            if (t >= 0 && token_row_offset(g, bt, t, 0, flags) < 0)
-                t = -1;
+            const int e = s >> 2, u = s & 3;
+            int first, page;
+            prefill_entry(g, bt, sel + (int64_t)r * n_sel, n_sel, pc >> 2, e, first, page, flags);
+            if (prefill_lane_live(page, e, n_sel, first, u, pc))
+                t = first + u;
         }
         dst[s] = t;
     }

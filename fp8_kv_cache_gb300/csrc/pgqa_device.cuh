@@ -112,13 +112,9 @@ struct KVGeom {
     int num_pages;
 };
 
-// Byte offset of the row of logical token t (KV head j) of the sequence whose
-// block-table row is bt_row, or -1 when its page id is outside [0, num_pages)
-// (then PAGED_GQA_FLAG_BAD_PAGE is added to *flags).
-__device__ __forceinline__ int64_t token_row_offset(const KVGeom& g, const int32_t* bt_row,
-                                                    int t, int j, int& flags)
+// Block-table index and slot of logical token t.
+__device__ __forceinline__ void page_and_slot(const KVGeom& g, int t, int& pi, int& slot)
 {
-    int pi, slot;
     if (g.page_shift >= 0) {
         pi = t >> g.page_shift;
         slot = t & ((1 << g.page_shift) - 1);
@@ -126,35 +122,75 @@ __device__ __forceinline__ int64_t token_row_offset(const KVGeom& g, const int32
         pi = t / g.page_size;
         slot = t - pi * g.page_size;
     }
+}
+
+// Physical page named by entry pi of the block-table row bt_row, or -1 when it
+// is outside [0, num_pages) (then PAGED_GQA_FLAG_BAD_PAGE is added to flags).
+__device__ __forceinline__ int table_page(const KVGeom& g, const int32_t* bt_row, int pi,
+                                          int& flags)
+{
     const int page = __ldg(bt_row + pi);
     if (page < 0 || page >= g.num_pages) {
         flags |= PAGED_GQA_FLAG_BAD_PAGE;
         return -1;
     }
+    return page;
+}
+
+// Byte offset of the row at (page, slot, KV head j).
+__device__ __forceinline__ int64_t row_offset(const KVGeom& g, int page, int slot, int j)
+{
     return (int64_t)page * g.page_b + (int64_t)slot * g.token_b + (int64_t)j * g.head_b;
 }
 
-// Logical token of lane u (0..3) of block entry `entry` of a sparse-prefill
-// row: entries 0..n_sel-1 are the selected four-token blocks, entry n_sel is
-// the row's own causal block, cut after position p.  -1 = not attended.
-__device__ __forceinline__ int prefill_token(const int32_t* sel_row, int n_sel, int own,
-                                             int p, int entry, int u, int& flags)
+// Byte offset of the row of logical token t (KV head j) of the sequence whose
+// block-table row is bt_row, or -1 when its page id is invalid.
+__device__ __forceinline__ int64_t token_row_offset(const KVGeom& g, const int32_t* bt_row,
+                                                    int t, int j, int& flags)
 {
-    if (entry < n_sel) {
-        const int b = __ldg(sel_row + entry);
+    int pi, slot;
+    page_and_slot(g, t, pi, slot);
+    const int page = table_page(g, bt_row, pi, flags);
+    return page < 0 ? -1 : row_offset(g, page, slot, j);
+}
+
+// Block entry e of a sparse-prefill row: entries 0..n_sel-1 are the selected
+// four-token blocks, entry n_sel is the row's own causal block.  Sets first
+// (the block's first logical token) and page (its physical page, or -1 when
+// the entry is not attended: padding, a block not strictly before the row's
+// own block (PAGED_GQA_FLAG_BAD_SEL), or an invalid page id).  A block never
+// straddles pages because page_size is a multiple of 4.
+__device__ __forceinline__ void prefill_entry(const KVGeom& g, const int32_t* bt,
+                                              const int32_t* sel_row, int n_sel, int own, int e,
+                                              int& first, int& page, int& flags)
+{
+    page = -1;
+    first = 0;
+    if (e < n_sel) {
+        const int b = __ldg(sel_row + e);
         if (b < 0)
-            return -1;                        // padding
+            return;                           // padding
         if (b >= own) {
             flags |= PAGED_GQA_FLAG_BAD_SEL;  // not strictly before the tail block
-            return -1;
+            return;
         }
-        return 4 * b + u;
+        first = 4 * b;
+    } else if (e == n_sel) {
+        first = 4 * own;
+    } else {
+        return;
     }
-    if (entry == n_sel) {
-        const int t = 4 * own + u;
-        return t <= p ? t : -1;
-    }
-    return -1;
+    int pi, slot;
+    page_and_slot(g, first, pi, slot);
+    page = table_page(g, bt, pi, flags);
+}
+
+// Whether lane u (0..3) of entry e is attended, given its page: every token
+// of a selected block, and the tail block's tokens up to the row's position p.
+__device__ __forceinline__ bool prefill_lane_live(int page, int e, int n_sel, int first, int u,
+                                                  int p)
+{
+    return page >= 0 && (e < n_sel || first + u <= p);
 }
 
 // ------------------------------------------------------------------ async ring
@@ -519,7 +555,12 @@ __device__ __forceinline__ void run_tiles(WarpCore<kE4M3>& wc, WarpRing<kE4M3, k
 
 // Shared-memory carve-up of a CTA of the attention kernels:
 //   [Q fragments (4 KB, shared)][rings of 4 warps (the merge buffer aliases them)]
-//   [stage masks][kernel-specific tail]
+//   [stage masks]
+//   [kernel-specific tail]
+// The sparse-prefill kernel keeps its address table in the tail: a chunk's
+// resolved block entries (int2 {first token, page} each), so that its ring
+// fills issue their copies without the two dependent global loads
+// (selection index, then block-table entry) in front of them.
 template <bool kE4M3>
 struct SmemPlan {
     static constexpr int kNS = kStages<kE4M3>();
@@ -527,6 +568,8 @@ struct SmemPlan {
     static constexpr size_t kRingBytes = (size_t)kWarps * kNS * Stage<kE4M3>::kBytes;
     static constexpr size_t kMaskOff = kQBytes + kRingBytes;
     static constexpr size_t kTailOff = (kMaskOff + (size_t)kWarps * kNS * 4 + 15) & ~(size_t)15;
+    static constexpr int kPrefillEntries = kE4M3 ? 520 : 1024; // block entries per prefill chunk
+    static constexpr size_t kPrefillSmem = kTailOff + (size_t)kPrefillEntries * sizeof(int2);
 };
 
 // ------------------------------------------------------------------ CTA merge

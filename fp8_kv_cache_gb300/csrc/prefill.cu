@@ -46,7 +46,6 @@ __global__ void __launch_bounds__(kThreads, kMinCtas<kE4M3>()) sparse_prefill_ke
             flags |= PAGED_GQA_FLAG_QPOS_CLAMPED;
     }
     const int own = p >> 2;
-    const int n_tiles = (a.n_sel + 1 + 3) / 4;   // selected entries + the tail entry, 4 per tile
     const int32_t* sel_row = a.sel + (size_t)r * a.n_sel;
 
     using Core = WarpCore<kE4M3>;
@@ -54,21 +53,42 @@ __global__ void __launch_bounds__(kThreads, kMinCtas<kE4M3>()) sparse_prefill_ke
     WarpRing<kE4M3, kStages<kE4M3>()> rg;
     rg.init(cs.ring, cs.masks);
     Core::stage_q(cs.qs, a.q + ((size_t)r * a.Hq + (size_t)j * a.G) * kD, a.G, lane, w);
-    __syncthreads();
     Core wc;
     wc.reset();
-    // half-tile h = block entries 2h, 2h+1 (8 tokens); lane t < 8 resolves token t
-    auto offset = [&](int h) -> int64_t {
-        if (lane < kHalf) {
-            const int t = prefill_token(sel_row, a.n_sel, own, p, 2 * h + (lane >> 2), lane & 3,
-                                        flags);
-            if (t >= 0)
-                return token_row_offset(a.kv, a.bt, t, j, flags);
+    // Chunks of block entries (selected blocks, then the tail entry): the CTA
+    // resolves a chunk's entries (selection index -> block -> page) into the
+    // address table first, so the ring fills need no dependent global load.
+    int2* tab = reinterpret_cast<int2*>(cs.tail);
+    constexpr int kCap = SmemPlan<kE4M3>::kPrefillEntries;   // a multiple of 4
+    const int n_entries = a.n_sel + 1;
+    for (int e0 = 0; e0 < n_entries; e0 += kCap) {
+        const int e1 = min(n_entries, e0 + kCap);
+        __syncthreads();                             // Q staged / previous chunk done with tab
+        for (int e = e0 + (int)threadIdx.x; e < e1; e += blockDim.x) {
+            int first, page;
+            prefill_entry(a.kv, a.bt, sel_row, a.n_sel, own, e, first, page, flags);
+            tab[e - e0] = make_int2(first, page);
         }
-        return -1;
-    };
-    run_tiles<kE4M3, kStages<kE4M3>()>(wc, rg, cs.qs, a.kv.k, a.kv.v, w, n_tiles, kWarps, a.G,
-                                       a.scale_log2, lane, offset);
+        __syncthreads();
+        // half-tile h = block entries 2h, 2h+1 (8 tokens); lane t < 8 takes token t
+        auto offset = [&](int h) -> int64_t {
+            if (lane < kHalf) {
+                const int e = 2 * h + (lane >> 2), u = lane & 3;
+                if (e < e1) {
+                    const int2 en = tab[e - e0];
+                    if (prefill_lane_live(en.y, e, a.n_sel, en.x, u, p)) {
+                        int pi, slot;
+                        page_and_slot(a.kv, en.x + u, pi, slot);
+                        return row_offset(a.kv, en.y, slot, j);
+                    }
+                }
+            }
+            return -1;
+        };
+        run_tiles<kE4M3, kStages<kE4M3>()>(wc, rg, cs.qs, a.kv.k, a.kv.v, e0 / 4 + w,
+                                           (e1 + 3) / 4, kWarps, a.G, a.scale_log2, lane,
+                                           offset);
+    }
     cta_merge<kE4M3>(*cs.merge, wc, a.G, a.v_scale, out_rows, nullptr);
     raise_flag(a.err, flags);
 }
@@ -86,7 +106,7 @@ static cudaError_t prefill_smem_attr()
         return cudaSuccess;
     e = cudaFuncSetAttribute(sparse_prefill_kernel<kE4M3>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)SmemPlan<kE4M3>::kTailOff);
+                             (int)SmemPlan<kE4M3>::kPrefillSmem);
     if (e == cudaSuccess && dev < kMaxDevices)
         done[dev].store(1, std::memory_order_release);
     return e;
@@ -99,9 +119,9 @@ cudaError_t launch_prefill(const PrefillArgs& a, bool e4m3, cudaStream_t s)
         return e;
     const dim3 grid(a.R, a.Hkv);
     if (e4m3)
-        sparse_prefill_kernel<true><<<grid, kThreads, SmemPlan<true>::kTailOff, s>>>(a);
+        sparse_prefill_kernel<true><<<grid, kThreads, SmemPlan<true>::kPrefillSmem, s>>>(a);
     else
-        sparse_prefill_kernel<false><<<grid, kThreads, SmemPlan<false>::kTailOff, s>>>(a);
+        sparse_prefill_kernel<false><<<grid, kThreads, SmemPlan<false>::kPrefillSmem, s>>>(a);
     return cudaGetLastError();
 }
 
