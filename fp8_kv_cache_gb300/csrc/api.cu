@@ -209,6 +209,7 @@ int paged_gqa_decode(const void* q, const void* k_cache, const void* v_cache,
         a.slots = reinterpret_cast<float*>(static_cast<unsigned char*>(ws->ptr) + head);
         a.C = C;
         a.min_tiles = ws->force_splits > 0 ? 0 : 8;
+        a.piece_cost = kPieceCostTiles;
     }
     void* ev0 = ws ? ws->split_events[0] : nullptr;
     void* ev1 = ws ? ws->split_events[1] : nullptr;

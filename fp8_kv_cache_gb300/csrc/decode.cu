@@ -5,15 +5,17 @@
 // batches of 1..16 including long contexts.
 //
 // Work decomposition (ours, not the page's V100 routing): every (sequence b,
-// KV head j) is a segment of ceil(L_b / 16) tiles; the segments are laid end
-// to end and the resulting tile line is cut into C_eff equal ranges, one per
-// CTA, so every CTA streams the same number of KV bytes whatever the mix of
-// sequence lengths.  The cut is computed on the device from seq_lens, so one
-// launch shape serves every step of a captured CUDA graph.  A CTA that covers
-// a whole segment writes the final FP16 rows; otherwise it writes an
-// unnormalised partial (m, l, O) to slot (cta + segment) of the caller's
-// workspace, and the merge kernel combines the pieces in a fixed order
-// (no floating-point atomics, so results are reproducible run to run).
+// KV head j) is a segment of ceil(L_b / 16) tiles, preceded on the line by
+// piece_cost virtual tiles that stand for the fixed cost of starting a piece;
+// the segments are laid end to end and the resulting line is cut into C_eff
+// equal ranges, one per CTA, so every CTA has the same amount of work (KV
+// bytes plus piece starts) whatever the mix of sequence lengths.  The cut is
+// computed on the device from seq_lens, so one launch shape serves every step
+// of a captured CUDA graph.  A CTA that covers all real tiles of a segment
+// writes the final FP16 rows; otherwise it writes an unnormalised partial
+// (m, l, O) to slot (cta + segment) of the caller's workspace, and the merge
+// kernel combines the pieces in a fixed order (no floating-point atomics, so
+// results are reproducible run to run).
 #include <atomic>
 
 #include "pgqa_internal.h"
@@ -119,13 +121,18 @@ __global__ void __launch_bounds__(kThreads, kMinCtas<kE4M3>()) decode_split_kern
     const int per = (a.B + kThreads - 1) / kThreads;
     const int b0 = min(a.B, tid * per), b1 = min(a.B, b0 + per);
     int64_t local = 0;
+    // line length of one segment of sequence b: its tiles plus the piece cost
+    auto seg_len = [&](int b) -> int64_t {
+        const int n = (clamp_len(__ldg(a.seq_lens + b), a.max_seq_len) + kTile - 1) / kTile;
+        return n > 0 ? (int64_t)n + a.piece_cost : 0;
+    };
     for (int b = b0; b < b1; ++b) {
         const int raw = __ldg(a.seq_lens + b);
         if (blockIdx.x == 0) {
             if (raw > a.max_seq_len) flags |= PAGED_GQA_FLAG_SEQ_CLAMPED;
             if (raw <= 0) flags |= PAGED_GQA_FLAG_EMPTY_ROW;
         }
-        local += (clamp_len(raw, a.max_seq_len) + kTile - 1) / kTile;
+        local += seg_len(b);
     }
     int64_t incl = local;
 #pragma unroll
@@ -143,7 +150,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas<kE4M3>()) decode_split_kern
     int64_t run = base + incl - local;
     for (int b = b0; b < b1; ++b) {
         P[b] = run;
-        run += (clamp_len(__ldg(a.seq_lens + b), a.max_seq_len) + kTile - 1) / kTile;
+        run += seg_len(b);
     }
     if (tid == 0) P[a.B] = total;
     __syncthreads();
@@ -177,16 +184,18 @@ __global__ void __launch_bounds__(kThreads, kMinCtas<kE4M3>()) decode_split_kern
     int j = (int)((x0 - (int64_t)a.Hkv * P[b]) / nb);
     for (;;) {
         const int64_t s0 = (int64_t)a.Hkv * P[b] + (int64_t)j * nb;
-        const int64_t s1 = s0 + nb;
         if (s0 >= x1)
             break;
-        const int ta = (int)(max(x0, s0) - s0), te = (int)(min(x1, s1) - s0);
-        const int L = clamp_len(__ldg(a.seq_lens + b), a.max_seq_len);
-        const int64_t k = (int64_t)b * a.Hkv + j;
-        const bool whole = x0 <= s0 && x1 >= s1;
-        __half* out_rows = whole ? a.out + ((size_t)b * a.Hq + (size_t)j * a.G) * kD : nullptr;
-        float* slot = whole ? nullptr : a.slots + (size_t)(c + k) * kSlotFloats;
-        run_piece<kE4M3>(a, cs, rg, b, j, L, ta, te, out_rows, slot, flags);
+        const int64_t r0 = s0 + a.piece_cost, r1 = s0 + nb;   // the segment's real tiles
+        if (max(x0, r0) < min(x1, r1)) {
+            const int ta = (int)(max(x0, r0) - r0), te = (int)(min(x1, r1) - r0);
+            const int L = clamp_len(__ldg(a.seq_lens + b), a.max_seq_len);
+            const int64_t k = (int64_t)b * a.Hkv + j;
+            const bool whole = x0 <= r0 && x1 >= r1;
+            __half* out_rows = whole ? a.out + ((size_t)b * a.Hq + (size_t)j * a.G) * kD : nullptr;
+            float* slot = whole ? nullptr : a.slots + (size_t)(c + k) * kSlotFloats;
+            run_piece<kE4M3>(a, cs, rg, b, j, L, ta, te, out_rows, slot, flags);
+        }
         // next non-empty segment
         if (++j == a.Hkv) {
             j = 0;
@@ -225,10 +234,11 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeArgs 
         out2[1] = __floats2half2_rn(0.f, 0.f);
         return;
     }
+    // CTAs c_first..c_last are the ones whose ranges meet the real tiles [r0, r1)
     const int64_t s0 = (int64_t)a.Hkv * P[b] + (int64_t)j * nb;
-    const int64_t s1 = s0 + nb;
-    const int64_t c_first = ((s0 + 1) * C + T - 1) / T - 1;
-    const int64_t c_last = (s1 * C + T - 1) / T - 1;
+    const int64_t r0 = s0 + a.piece_cost, r1 = s0 + nb;
+    const int64_t c_first = ((r0 + 1) * C + T - 1) / T - 1;
+    const int64_t c_last = (r1 * C + T - 1) / T - 1;
     if (c_first == c_last)
         return;
     const int64_t k = (int64_t)b * a.Hkv + j;

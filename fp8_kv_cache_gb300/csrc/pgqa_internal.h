@@ -13,6 +13,12 @@ constexpr int kMaxSplitBatch = 4096;   // split route keeps a (B+1) prefix in sh
 constexpr int kMergeThreads = 64;     // 4 head-dim values per thread
 constexpr int kHeaderBytes = 64;       // workspace header: T, C_eff
 constexpr int kMaxDevices = 64;        // per-device caches
+// Virtual tiles charged at the start of every non-empty segment when the tile
+// line is cut among the split CTAs: a CTA whose range takes in a segment start
+// runs one more piece (Q staging, pipeline start, CTA merge, about 5 us at
+// full load against 0.56 us per tile per CTA), so such CTAs get that much less
+// real work.  8 to 20 were measured; 12 to 20 tie and beat 0 by about 4%.
+constexpr int kPieceCostTiles = 12;
 
 struct DecodeArgs {
     const __half* q;
@@ -25,10 +31,11 @@ struct DecodeArgs {
     float v_scale;       // kv_scale for E4M3 V, 1 for FP16
     __half* out;
     // split route only
-    int64_t* hdr;        // [0] = T (tiles), [1] = C_eff, then prefix[B + 1]
+    int64_t* hdr;        // [0] = T (line length), [1] = C_eff, then prefix[B + 1]
     float* slots;        // (C + B * Hkv) partial slots
     int C;               // CTAs launched on the split route; 0 = unsplit route
     int min_tiles;       // minimum tiles per CTA when choosing C_eff
+    int piece_cost;      // virtual tiles at the start of each non-empty segment
     int* err;
 };
 
