@@ -43,6 +43,25 @@ __device__ __forceinline__ int find_seq(const int64_t* P, int B, int Hkv, int64_
     return lo;
 }
 
+// Line length of one segment of sequence b: its tiles plus the piece cost
+// (0 for an empty sequence).
+__device__ __forceinline__ int64_t seg_len(const DecodeArgs& a, int b)
+{
+    const int n = (clamp_len(__ldg(a.seq_lens + b), a.max_seq_len) + kTile - 1) / kTile;
+    return n > 0 ? (int64_t)n + a.piece_cost : 0;
+}
+
+// CTAs that take part in the cut of a line of T > 0 tiles: at most the
+// launched C, at most ceil(T / min_tiles) when min_tiles > 0, and at most T,
+// so every one of them gets a non-empty range.
+__device__ __forceinline__ int64_t effective_ctas(const DecodeArgs& a, int64_t T)
+{
+    int64_t C = a.C;
+    if (a.min_tiles > 0)
+        C = min(C, (T + a.min_tiles - 1) / a.min_tiles);
+    return max((int64_t)1, min(C, T));
+}
+
 // The tiles [ta, te) of segment (b, j) processed by this CTA's warps
 // (16-token tiles, round-robin), then merged into out_rows (final) or slot
 // (partial).  CTA-uniform: every thread of the CTA calls it.
@@ -121,18 +140,13 @@ __global__ void __launch_bounds__(kThreads, kMinCtas<kE4M3>()) decode_split_kern
     const int per = (a.B + kThreads - 1) / kThreads;
     const int b0 = min(a.B, tid * per), b1 = min(a.B, b0 + per);
     int64_t local = 0;
-    // line length of one segment of sequence b: its tiles plus the piece cost
-    auto seg_len = [&](int b) -> int64_t {
-        const int n = (clamp_len(__ldg(a.seq_lens + b), a.max_seq_len) + kTile - 1) / kTile;
-        return n > 0 ? (int64_t)n + a.piece_cost : 0;
-    };
     for (int b = b0; b < b1; ++b) {
         const int raw = __ldg(a.seq_lens + b);
         if (blockIdx.x == 0) {
             if (raw > a.max_seq_len) flags |= PAGED_GQA_FLAG_SEQ_CLAMPED;
             if (raw <= 0) flags |= PAGED_GQA_FLAG_EMPTY_ROW;
         }
-        local += seg_len(b);
+        local += seg_len(a, b);
     }
     int64_t incl = local;
 #pragma unroll
@@ -150,18 +164,14 @@ __global__ void __launch_bounds__(kThreads, kMinCtas<kE4M3>()) decode_split_kern
     int64_t run = base + incl - local;
     for (int b = b0; b < b1; ++b) {
         P[b] = run;
-        run += seg_len(b);
+        run += seg_len(a, b);
     }
     if (tid == 0) P[a.B] = total;
     __syncthreads();
 
     const int64_t T = (int64_t)a.Hkv * total;
-    int64_t C = a.C;
-    if (a.min_tiles > 0) {
-        const int64_t want = (T + a.min_tiles - 1) / a.min_tiles;
-        C = max((int64_t)1, min(C, want));
-    }
-    if (blockIdx.x == 0) {
+    const int64_t C = T > 0 ? effective_ctas(a, T) : 0;
+    if (blockIdx.x == 0 && a.B > kMergeScanMax) {
         for (int i = tid; i <= a.B; i += kThreads)
             a.hdr[2 + i] = P[i];
         if (tid == 0) {
@@ -174,11 +184,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas<kE4M3>()) decode_split_kern
         raise_flag(a.err, flags);
         return;
     }
-    const int64_t x0 = c * T / C, x1 = (c + 1) * T / C;
-    if (x0 >= x1) {
-        raise_flag(a.err, flags);
-        return;
-    }
+    const int64_t x0 = c * T / C, x1 = (c + 1) * T / C;   // non-empty: C <= T
     int b = find_seq(P, a.B, a.Hkv, x0);
     int64_t nb = P[b + 1] - P[b];
     int j = (int)((x0 - (int64_t)a.Hkv * P[b]) / nb);
@@ -214,89 +220,107 @@ __global__ void __launch_bounds__(kThreads, kMinCtas<kE4M3>()) decode_split_kern
 // head-dim values each): zero rows for empty sequences, nothing for segments
 // one split CTA covered, else the fixed-order LSE merge of the pieces
 //   M = max m_i,  O = sum_i 2^(m_i - M) O_i / sum_i 2^(m_i - M) l_i.
-// The pieces' (m, l) go through shared memory first so that every O load
-// can be in flight at once.  Launched as a programmatic dependent of the
-// split kernel: it may start early and waits on griddepcontrol.wait.
+// Launched as a programmatic dependent of the split kernel, it is resident
+// before the split kernel ends, so everything that depends only on seq_lens
+// (the cut, hence which CTAs hold the segment's pieces) is done before
+// griddepcontrol.wait; after it, one round of loads brings every piece's
+// (m, l, O) in.  Batches above kMergeScanMax read the prefix the split kernel
+// leaves in the workspace header instead, after the wait.
 __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeArgs a)
 {
-    __shared__ float w_s[kMergeThreads];
-    __shared__ float red_s[2];
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    __shared__ int64_t red_s[2][2];
     const int h = blockIdx.x, b = blockIdx.y;
     const int j = h / a.G, hh = h - j * a.G;
     const int tid = threadIdx.x, d = 4 * tid;
-    const int64_t T = a.hdr[0], C = a.hdr[1];
-    const int64_t* P = a.hdr + 2;
-    const int64_t nb = P[b + 1] - P[b];
     __half2* out2 = reinterpret_cast<__half2*>(a.out + ((size_t)b * a.Hq + h) * kD + d);
-    if (nb == 0) {
+    int64_t before, total;     // line tiles of sequences < b, of all sequences
+    if (a.B <= kMergeScanMax) {
+        int64_t lo = 0, all = 0;
+        for (int i = tid; i < a.B; i += kMergeThreads) {
+            const int64_t n = seg_len(a, i);
+            all += n;
+            lo += i < b ? n : 0;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            lo += __shfl_xor_sync(0xffffffffu, lo, o);
+            all += __shfl_xor_sync(0xffffffffu, all, o);
+        }
+        if ((tid & 31) == 0) {
+            red_s[tid >> 5][0] = lo;
+            red_s[tid >> 5][1] = all;
+        }
+        __syncthreads();
+        before = red_s[0][0] + red_s[1][0];
+        total = red_s[0][1] + red_s[1][1];
+    } else {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        before = a.hdr[2 + b];
+        total = a.hdr[2 + a.B];
+    }
+    // Every CTA waits for the split grid before it exits, so that the end of
+    // this grid always implies the end of the split grid.
+    const int64_t nb = seg_len(a, b);
+    if (nb == 0) {                               // the split kernel never writes these rows
         out2[0] = __floats2half2_rn(0.f, 0.f);
         out2[1] = __floats2half2_rn(0.f, 0.f);
+        asm volatile("griddepcontrol.wait;" ::: "memory");
         return;
     }
+    const int64_t T = (int64_t)a.Hkv * total;
+    const int64_t C = effective_ctas(a, T);
     // CTAs c_first..c_last are the ones whose ranges meet the real tiles [r0, r1)
-    const int64_t s0 = (int64_t)a.Hkv * P[b] + (int64_t)j * nb;
+    const int64_t s0 = (int64_t)a.Hkv * before + (int64_t)j * nb;
     const int64_t r0 = s0 + a.piece_cost, r1 = s0 + nb;
     const int64_t c_first = ((r0 + 1) * C + T - 1) / T - 1;
     const int64_t c_last = (r1 * C + T - 1) / T - 1;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (c_first == c_last)
-        return;
+        return;                                  // one split CTA wrote the final rows
     const int64_t k = (int64_t)b * a.Hkv + j;
     const float* base = a.slots + (size_t)(c_first + k) * kSlotFloats;
     float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
     float den = 0.f, M_run = -INFINITY;
-    // pieces in chunks of kMergeThreads: thread i loads (m, l) of piece c0 + i
-    for (int64_t c0 = c_first; c0 <= c_last; c0 += kMergeThreads) {
-        const int np = (int)min((int64_t)kMergeThreads, c_last - c0 + 1);
-        float m_i = -INFINITY, l_i = 0.f;
-        if (tid < np) {
-            const int64_t c = c0 + tid;
-            // CTAs with an empty tile range (possible when C > T) wrote no slot.
-            if (c * T / C != (c + 1) * T / C) {
-                const float* sl = base + (size_t)(c - c_first) * kSlotFloats;
-                m_i = sl[hh];
-                l_i = sl[kGMax + hh];
+    constexpr int kChunk = 8;
+    for (int64_t c0 = c_first; c0 <= c_last; c0 += kChunk) {
+        const int np = (int)min((int64_t)kChunk, c_last - c0 + 1);
+        const float* sl0 = base + (size_t)(c0 - c_first) * kSlotFloats;
+        float m[kChunk], l[kChunk];
+        float4 o[kChunk];
+#pragma unroll
+        for (int i = 0; i < kChunk; ++i) {
+            m[i] = -INFINITY;
+            l[i] = 0.f;
+            o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (i < np) {
+                const float* sl = sl0 + (size_t)i * kSlotFloats;
+                m[i] = sl[hh];
+                l[i] = sl[kGMax + hh];
+                o[i] = *reinterpret_cast<const float4*>(sl + 2 * kGMax + hh * kD + d);
             }
         }
-        float mx = m_i;
-        for (int o = 16; o > 0; o >>= 1)
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        if ((tid & 31) == 0)
-            red_s[tid >> 5] = mx;
-        __syncthreads();
-        const float M_new = fmaxf(M_run, fmaxf(red_s[0], red_s[1]));
-        __syncthreads();
-        if (M_new == -INFINITY)
-            continue;                        // nothing attended so far (CTA-uniform)
-        const float carry = (M_run == -INFINITY) ? 0.f : ex2(M_run - M_new);
+        float M = M_run;
+#pragma unroll
+        for (int i = 0; i < kChunk; ++i)
+            M = fmaxf(M, m[i]);
+        if (M == -INFINITY)
+            continue;                            // nothing attended so far
+        const float carry = (M_run == -INFINITY) ? 0.f : ex2(M_run - M);
         num.x *= carry;
         num.y *= carry;
         num.z *= carry;
         num.w *= carry;
         den *= carry;
-        M_run = M_new;
-        const float wi = (m_i == -INFINITY) ? 0.f : ex2(m_i - M_new);
-        w_s[tid] = wi;
-        float part = wi * l_i;
-        for (int o = 16; o > 0; o >>= 1)
-            part += __shfl_xor_sync(0xffffffffu, part, o);
-        if ((tid & 31) == 0)
-            red_s[tid >> 5] = part;
-        __syncthreads();
-        den += red_s[0] + red_s[1];
-        const float* o_base = base + (size_t)(c0 - c_first) * kSlotFloats + 2 * kGMax + hh * kD + d;
-#pragma unroll 8
-        for (int i = 0; i < np; ++i) {
-            const float e = w_s[i];
-            if (e != 0.f) {
-                const float4 o = *reinterpret_cast<const float4*>(o_base + (size_t)i * kSlotFloats);
-                num.x += e * o.x;
-                num.y += e * o.y;
-                num.z += e * o.z;
-                num.w += e * o.w;
-            }
+        M_run = M;
+#pragma unroll
+        for (int i = 0; i < kChunk; ++i) {
+            const float e = (m[i] == -INFINITY) ? 0.f : ex2(m[i] - M);
+            den += e * l[i];
+            num.x += e * o[i].x;
+            num.y += e * o[i].y;
+            num.z += e * o[i].z;
+            num.w += e * o[i].w;
         }
-        __syncthreads();                     // w_s and red_s are reused by the next chunk
     }
     const float sc = den > 0.f ? a.v_scale / den : 0.f;
     out2[0] = __floats2half2_rn(num.x * sc, num.y * sc);

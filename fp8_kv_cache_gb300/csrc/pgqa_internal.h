@@ -11,6 +11,7 @@ namespace pgqa {
 
 constexpr int kMaxSplitBatch = 4096;   // split route keeps a (B+1) prefix in shared memory
 constexpr int kMergeThreads = 64;     // 4 head-dim values per thread
+constexpr int kMergeScanMax = 512;    // merge recomputes the cut from seq_lens up to this batch
 constexpr int kHeaderBytes = 64;       // workspace header: T, C_eff
 constexpr int kMaxDevices = 64;        // per-device caches
 // Virtual tiles charged at the start of every non-empty segment when the tile

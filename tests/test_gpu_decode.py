@@ -109,6 +109,22 @@ def test_split_count_invariance(splits):
     U.assert_close(got, ref, f"splits={splits} vs automatic")
 
 
+@pytest.mark.parametrize("kvd", ["fp16", "e4m3"])
+@pytest.mark.parametrize("B", [512, 513, 1500])
+def test_large_batches(B, kvd):
+    """Batches on both sides of 512, where the merge kernel switches from
+    recomputing the cut from seq_lens to reading the prefix the split kernel
+    leaves in the workspace; short ragged lengths with empty rows."""
+    rng = np.random.default_rng(1000 + B)
+    lens = rng.integers(-2, 200, size=B).astype(np.int32)
+    c = W.decode_case(f"large_b{B}", B=B, Hq=12, Hkv=2, seq_lens=lens, kv_dtype=kvd,
+                      seed=95 + B, max_seq_len=200)
+    got = _check_full(c)
+    for splits in (B // 3, 4 * B):
+        alt, _ = U.run_decode(c, force_splits=splits)
+        U.assert_close(alt, got, f"B={B} splits={splits} vs automatic")
+
+
 def test_inert_inputs_match_oracle():
     c = W.decode_case("inert", B=6, Hq=12, Hkv=2, seq_lens=[40, 0, -3, 500, 64, 33],
                       kv_dtype="e4m3", seed=91, max_seq_len=256, num_pages=200)
