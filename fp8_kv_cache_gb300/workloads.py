@@ -14,7 +14,13 @@ Shapes and value distributions follow the workloads the pages describe:
 * sparse prefill: Hq6/Hkv1/D256 FP16, 4096 query rows, each attending to 512
   selected four-token blocks plus a causal tail of 1..3 tokens, contiguous or
   interleaved K/V ("[Kernel][SM70] Accelerate Qwen3.8 QSA paged prefill",
-  Changes and Test Result).
+  Changes and Test Result);
+* block selection: float32 block scores of the same 4096 rows, from which 512
+  blocks per row are selected ("[Kernel][SM70] Accelerate exact Qwen3.8
+  decode", Implementation).  The pages' scores come from a trained scorer,
+  which is out of reach here; the stand-in draws N(0,1) values rounded to
+  bfloat16 precision (through torch's bfloat16 cast), so equal scores at the
+  selection pivot are common, as the page's tie rule anticipates.
 
 E4M3 quantisation of the drawn values uses torch's float8_e4m3fn cast (a
 library routine; round to nearest even) after dividing by the per-tensor scale
@@ -260,3 +266,45 @@ def sparse_prefill_4096(seed=5, interleaved=True, R=4096):
     attends to 512 selected blocks plus a tail of 1..3 tokens."""
     return prefill_case(f"sparse_prefill_r{R}", R=R, n_sel=512, seed=seed, first_block=4096,
                         kv_len=32768, interleaved=interleaved)
+
+
+@dataclass
+class SelectCase:
+    """Inputs of one block-selection call: scores [R, score_stride] float32
+    (the first n_blocks columns are used), q_pos int32 [R]."""
+    name: str
+    scores: np.ndarray
+    q_pos: np.ndarray
+    kv_len: int
+    k: int
+    n_blocks: int
+
+
+def select_case(name, *, R, n_blocks, k, seed, kv_len=None, first_block=None, q_pos=None,
+                score_stride=None, bf16_ties=True):
+    """Scores N(0,1) (rounded to bfloat16 precision when ``bf16_ties``) for R
+    rows; row r sits at q_pos[r] (default: owns block first_block + r with a
+    tail of 1..3 tokens, as in the prefill workload)."""
+    rng = np.random.default_rng(seed)
+    stride = n_blocks if score_stride is None else score_stride
+    x = rng.standard_normal((R, stride)).astype(np.float32)
+    if bf16_ties:
+        import torch
+        x = torch.from_numpy(x).to(torch.bfloat16).to(torch.float32).numpy()
+    if q_pos is None:
+        fb = k if first_block is None else first_block
+        own = fb + np.arange(R, dtype=np.int64)
+        q_pos = 4 * own + rng.integers(0, 3, size=R)
+    q_pos = np.asarray(q_pos, dtype=np.int32).reshape(R)
+    if kv_len is None:
+        kv_len = int(q_pos.max()) + 1 if R else 1
+    return SelectCase(name=name, scores=np.ascontiguousarray(x), q_pos=q_pos, kv_len=int(kv_len),
+                      k=int(k), n_blocks=int(n_blocks))
+
+
+def qsa_select_4096(seed=6, R=4096):
+    """The 4096 rows of the sparse-prefill workload (row r owns block
+    4096 + r, 32768-token cache, so 8192 blocks): select 512 of the blocks
+    before each row's own, from bfloat16-precision N(0,1) scores."""
+    return select_case(f"qsa_select_r{R}", R=R, n_blocks=8192, k=512, seed=seed, kv_len=32768,
+                       first_block=4096)

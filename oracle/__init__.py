@@ -10,7 +10,9 @@ follows (1Cat-vLLM pull requests):
 
 * decode: "[Kernel][SM70] Scale NVFP4 E4M3 decode batches" (#282), Purpose;
 * sparse prefill and the inert-input rules: "[Kernel][SM70] Accelerate Qwen3.8
-  QSA paged prefill" (#378), Changes.
+  QSA paged prefill" (#378), Changes;
+* QSA block selection (top-k of block scores, ties to the lower index):
+  "[Kernel][SM70] Accelerate exact Qwen3.8 decode" (#415), Implementation.
 
 ``Oracle(path)`` loads any compiled copy of the source (the tests use this to
 check that deliberately broken copies fail the pins); the module-level
@@ -35,6 +37,7 @@ FLAG_SEQ_CLAMPED = 2
 FLAG_EMPTY_ROW = 4
 FLAG_QPOS_CLAMPED = 8
 FLAG_BAD_SEL = 16
+FLAG_SCORES_SHORT = 32
 
 
 def compile_source(src: str, out: str) -> str:
@@ -111,6 +114,8 @@ class Oracle:
         lib.orc_gather_rows.restype = i32
         lib.orc_sparse_row_tokens.argtypes = [vp, i32, i32, vp, i32, ctypes.c_int32, i32, vp, i64]
         lib.orc_sparse_row_tokens.restype = i64
+        lib.orc_select_blocks.argtypes = [vp, i64, i32, vp, i32, i32, i32, vp, vp, i32]
+        lib.orc_select_blocks.restype = i32
         self.lib = lib
         self.path = path
 
@@ -198,6 +203,25 @@ class Oracle:
             raise ValueError("token buffer too small")
         return buf[:n].copy()
 
+    def select_blocks(self, scores, q_pos, kv_len, k, n_blocks=None, threads=None):
+        """QSA block selection.  scores float32 [R, >= n_blocks] (row stride
+        taken from the array); q_pos int32 [R].  Returns (sel int32 [R, k],
+        flags)."""
+        sc = np.asarray(scores, dtype=np.float32)
+        if sc.ndim != 2 or sc.strides[1] != 4:
+            raise ValueError("scores must be 2-D float32 with unit column stride")
+        R = sc.shape[0]
+        n_blocks = sc.shape[1] if n_blocks is None else int(n_blocks)
+        qp = np.ascontiguousarray(q_pos, dtype=np.int32).reshape(R)
+        sel = np.empty((R, int(k)), dtype=np.int32)
+        flags = ctypes.c_int(0)
+        rc = self.lib.orc_select_blocks(sc.ctypes.data, sc.strides[0] // 4, n_blocks, _ptr(qp), R,
+                                        int(kv_len), int(k), sel.ctypes.data,
+                                        ctypes.addressof(flags), threads or default_threads())
+        if rc != 0:
+            raise ValueError("oracle rejected the selection shapes" if rc == -1 else "out of memory")
+        return sel, flags.value
+
     def gather_rows(self, cache, block_table, seq_lens, page_size, num_pages, max_seq_len,
                     kv_scale=1.0, T=None, threads=None):
         """Gathered, dequantised rows [B, T, Hkv, D] float32 of one K or V pool
@@ -245,3 +269,7 @@ def sparse_row_tokens(*args, **kwargs):
 
 def gather_rows(*args, **kwargs):
     return default().gather_rows(*args, **kwargs)
+
+
+def select_blocks(*args, **kwargs):
+    return default().select_blocks(*args, **kwargs)

@@ -18,6 +18,11 @@
  *       last; block tables in physical-page units; contiguous or interleaved
  *       K/V strides; padded or stale positions clamped to the live length and
  *       invalid requests made inert.
+ *   [S] "[Kernel][SM70] Accelerate exact Qwen3.8 decode" (#415),
+ *       Implementation and Focused tests: QSA's block selection, a radix
+ *       selection over the block scores whose ties at the pivot go to the
+ *       lower block index, checked for GPU exactness; its output is the
+ *       selected-block list that [P] consumes.
  *
  * The method is exact softmax attention over a defined token set, so this
  * oracle is that definition written out in FP64:
@@ -56,6 +61,7 @@
 #define ORC_FLAG_EMPTY_ROW    4  /* seq_len <= 0 or q_pos < 0: zero output row   */
 #define ORC_FLAG_QPOS_CLAMPED 8  /* q_pos >= kv_len, clamped to kv_len - 1       */
 #define ORC_FLAG_BAD_SEL     16  /* selected block at/after the tail block       */
+#define ORC_FLAG_SCORES_SHORT 32  /* a row's candidates exceed the scores given   */
 
 /* ------------------------------------------------------------------------- */
 /* Number formats                                                              */
@@ -440,4 +446,122 @@ int64_t orc_sparse_row_tokens(const int32_t* block_table, int num_pages, int kv_
         tokens[n++] = t;
     }
     return n;
+}
+
+/* ------------------------------------------------------------------------- */
+/* QSA block selection [S]                                                     */
+/* ------------------------------------------------------------------------- */
+/*
+ * The result the radix selection of [S] reaches is a plain top-k, so the
+ * oracle is that definition written out: sort a row's candidate blocks best
+ * first (greater score first, equal scores by increasing block index), keep
+ * the first min(k, n), and list them by increasing block index, padded with
+ * -1 to k entries.
+ *
+ * Readings taken where the pages are silent (listed in the design doc):
+ *   - the candidates of a row at position p are the blocks strictly before its
+ *     own block, 0 .. floor(p / 4) - 1, the blocks [P] accepts in a selection;
+ *     p is q_pos clamped to kv_len - 1 as in [P] (ORC_FLAG_QPOS_CLAMPED);
+ *   - q_pos < 0 or kv_len <= 0 gives a row of -1 (ORC_FLAG_EMPTY_ROW);
+ *   - only the n_blocks scores a row provides can be candidates
+ *     (ORC_FLAG_SCORES_SHORT when floor(p / 4) > n_blocks);
+ *   - scores are binary32 compared by IEEE 754 totalOrder, which orders every
+ *     bit pattern: -NaN < -inf < negatives < -0 < +0 < positives < +inf < +NaN.
+ */
+
+/* totalOrder of two binary32 values given by their bit patterns: a value
+ * with the sign bit set is below one without; among values without it, a
+ * larger encoding (greater magnitude, then infinity, then NaN payloads) is
+ * greater, and among values with it the larger encoding is smaller.
+ * Returns -1 (a below b), 0 (same pattern) or 1. */
+static int orc_total_order_cmp(uint32_t a, uint32_t b)
+{
+    const int neg_a = (int)(a >> 31), neg_b = (int)(b >> 31);
+    if (neg_a != neg_b)
+        return neg_a ? -1 : 1;
+    if (a == b)
+        return 0;
+    if (!neg_a)
+        return a < b ? -1 : 1;
+    return a > b ? -1 : 1;
+}
+
+typedef struct {
+    uint32_t bits;   /* the score's bit pattern */
+    int32_t idx;     /* its block index */
+} orc_cand;
+
+/* qsort order of candidates: best first; equal scores by increasing index. */
+static int orc_cand_best_first(const void* x, const void* y)
+{
+    const orc_cand* a = (const orc_cand*)x;
+    const orc_cand* b = (const orc_cand*)y;
+    const int c = orc_total_order_cmp(a->bits, b->bits);
+    if (c != 0)
+        return -c;
+    return (a->idx > b->idx) - (a->idx < b->idx);
+}
+
+static int orc_int32_ascending(const void* x, const void* y)
+{
+    const int32_t a = *(const int32_t*)x, b = *(const int32_t*)y;
+    return (a > b) - (a < b);
+}
+
+/* scores: R rows of score_stride floats, the first n_blocks of each used;
+ * q_pos int32 [R]; sel_out int32 [R, k].  Returns 0, -1 on bad shapes or -2
+ * when memory runs out. */
+int orc_select_blocks(const float* scores, int64_t score_stride, int n_blocks,
+                      const int32_t* q_pos, int R, int kv_len, int k, int32_t* sel_out,
+                      int* flags, int n_threads)
+{
+    if (R < 0 || k < 0 || n_blocks < 0 || score_stride < n_blocks)
+        return -1;
+    int fl = 0, oom = 0;
+#pragma omp parallel for num_threads(n_threads) schedule(dynamic, 8) reduction(|:fl, oom)
+    for (int r = 0; r < R; ++r) {
+        int32_t* out = sel_out + (int64_t)r * k;
+        for (int i = 0; i < k; ++i)
+            out[i] = -1;
+        int64_t p = q_pos[r];
+        if (p < 0 || kv_len <= 0) {
+            fl |= ORC_FLAG_EMPTY_ROW;
+            continue;
+        }
+        if (p >= kv_len) {
+            fl |= ORC_FLAG_QPOS_CLAMPED;
+            p = kv_len - 1;
+        }
+        int64_t n = p / 4;                      /* blocks strictly before its own */
+        if (n > n_blocks) {
+            fl |= ORC_FLAG_SCORES_SHORT;
+            n = n_blocks;
+        }
+        if (n == 0 || k == 0)
+            continue;
+        orc_cand* cand = (orc_cand*)malloc((size_t)n * sizeof(orc_cand));
+        int32_t* pick = (int32_t*)malloc((size_t)n * sizeof(int32_t));
+        if (cand == NULL || pick == NULL) {
+            free(cand);
+            free(pick);
+            oom = 1;
+            continue;
+        }
+        const float* row = scores + (int64_t)r * score_stride;
+        for (int64_t i = 0; i < n; ++i) {
+            memcpy(&cand[i].bits, &row[i], sizeof(uint32_t));
+            cand[i].idx = (int32_t)i;
+        }
+        qsort(cand, (size_t)n, sizeof(orc_cand), orc_cand_best_first);
+        const int64_t m = n < k ? n : k;
+        for (int64_t i = 0; i < m; ++i)
+            pick[i] = cand[i].idx;
+        qsort(pick, (size_t)m, sizeof(int32_t), orc_int32_ascending);
+        memcpy(out, pick, (size_t)m * sizeof(int32_t));
+        free(cand);
+        free(pick);
+    }
+    if (flags != NULL)
+        *flags |= fl;
+    return oom ? -2 : 0;
 }

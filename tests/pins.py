@@ -8,7 +8,11 @@ when it disagrees with:
   * invariants of softmax attention (convex hull, page-permutation invariance,
     one-token context, equal keys, zero query, split/merge identity),
   * the selected-sparse layout printed on the page (2051 tokens for 512 blocks
-    plus a 3-token tail) and the dense causal special case.
+    plus a 3-token tail) and the dense causal special case,
+  * for the block selection: numpy's stable argsort (ties to the lower index)
+    on finite scores, closed forms (monotone and constant rows, k >= n), an
+    IEEE totalOrder case written out by hand, the inert-row rules, and a
+    brute-force dominance check over every subset of tiny rows.
 ``ALL_PINS`` runs them all; test_oracle.py runs each one on the committed
 oracle and test_oracle_mutants.py checks that broken copies fail some pin.
 """
@@ -413,6 +417,109 @@ def pin_prefill_inert(o):
     _close(got[2], refs.dense_prefill_row(c2, 2), what="skipped blocks")
 
 
+# ---------------------------------------------------------------- block selection
+
+def _sel_positions(n_cands, rng=None):
+    """q_pos values whose rows have exactly n_cands candidate blocks."""
+    n_cands = np.asarray(n_cands, dtype=np.int64)
+    tail = np.zeros_like(n_cands) if rng is None else rng.integers(0, 4, size=n_cands.shape)
+    return (4 * n_cands + tail).astype(np.int32)
+
+
+def pin_select_library(o):
+    """Finite scores with many ties: the top k of the first floor(p/4) blocks
+    are numpy's stable argsort of -score (equal scores keep increasing index
+    order), sorted ascending."""
+    rng = np.random.default_rng(61)
+    R, nb = 64, 300
+    sc = rng.integers(1, 40, size=(R, nb)).astype(np.float32) * 0.25   # no zeros, many ties
+    sc[:, ::7] *= -1.0
+    n = rng.integers(0, nb + 1, size=R)
+    qp = _sel_positions(n, rng)
+    for k in (1, 5, 64, 299, 400):
+        got, flags = o.select_blocks(sc, qp, kv_len=4 * nb + 4, k=k)
+        assert flags == 0
+        for r in range(R):
+            top = np.sort(np.argsort(-sc[r, :n[r]], kind="stable")[:k])
+            want = np.full(k, -1, dtype=np.int32)
+            want[:top.size] = top
+            assert np.array_equal(got[r], want), (k, r)
+
+
+def pin_select_closed_forms(o):
+    """Increasing scores keep the last k candidates, decreasing the first k,
+    constant rows the first k (ties go to the lower index); k >= n keeps all."""
+    n, k = 50, 8
+    inc = np.arange(1, n + 1, dtype=np.float32)
+    sc = np.stack([inc, inc[::-1].copy(), np.full(n, 3.5, np.float32)])
+    qp = _sel_positions([n, n, n])
+    got, _ = o.select_blocks(sc, qp, kv_len=4 * n + 4, k=k)
+    assert np.array_equal(got[0], np.arange(n - k, n)), got[0]
+    assert np.array_equal(got[1], np.arange(k)), got[1]
+    assert np.array_equal(got[2], np.arange(k)), got[2]
+    got, _ = o.select_blocks(sc, _sel_positions([3, 0, 50]), kv_len=4 * n + 4, k=60)
+    assert np.array_equal(got[0], np.r_[0, 1, 2, [-1] * 57])
+    assert np.all(got[1] == -1)
+    assert np.array_equal(got[2], np.r_[np.arange(50), [-1] * 10])
+
+
+def pin_select_total_order(o):
+    """A row holding +0, -0, +NaN, -inf, 1, -NaN, +inf, -1 (indices 0..7).
+    IEEE totalOrder ranks them +NaN > +inf > 1 > +0 > -0 > -1 > -inf > -NaN,
+    so the top k for k = 1..8 are, by hand:"""
+    bits = np.array([0x00000000, 0x80000000, 0x7FC00000, 0xFF800000,
+                     0x3F800000, 0xFFC00000, 0x7F800000, 0xBF800000], dtype=np.uint32)
+    sc = bits.view(np.float32).reshape(1, 8)
+    want = {1: [2], 2: [2, 6], 3: [2, 4, 6], 4: [0, 2, 4, 6], 5: [0, 1, 2, 4, 6],
+            6: [0, 1, 2, 4, 6, 7], 7: [0, 1, 2, 3, 4, 6, 7], 8: list(range(8))}
+    for k, w in want.items():
+        got, _ = o.select_blocks(sc, _sel_positions([8]), kv_len=64, k=k)
+        assert got[0].tolist() == w, (k, got[0].tolist())
+
+
+def pin_select_inert(o):
+    """q_pos < 0 or kv_len <= 0: a row of -1 and the empty-row bit; q_pos at or
+    past kv_len is clamped to kv_len - 1 (bit 8); positions 0..3 have no
+    candidate; more candidates than scores are cut to the scores (bit 32)."""
+    rng = np.random.default_rng(62)
+    sc = rng.standard_normal((6, 40)).astype(np.float32)
+    qp = np.array([-1, 0, 3, 500, 77, 60], dtype=np.int32)
+    got, flags = o.select_blocks(sc, qp, kv_len=100, k=6)
+    assert flags == 4 | 8, flags
+    assert np.all(got[:3] == -1)
+    clamped, _ = o.select_blocks(sc[3:4], [99], kv_len=100, k=6)   # 24 candidates
+    assert np.array_equal(got[3], clamped[0])
+    sc[5, 39] = 100.0                                             # the best block is the last
+    short, _ = o.select_blocks(sc[5:6], [159], kv_len=1000, k=6)   # 39 candidates < 50
+    cut, f2 = o.select_blocks(sc[5:6], [200], kv_len=1000, k=6)    # 50 candidates > 40
+    full, _ = o.select_blocks(sc[5:6], [160], kv_len=1000, k=6)    # exactly 40
+    assert f2 == 32 and np.array_equal(cut, full) and not np.array_equal(short, full)
+    none, f3 = o.select_blocks(sc[:2], [5, 9], kv_len=0, k=3)
+    assert f3 == 4 and np.all(none == -1)
+
+
+def pin_select_brute_force(o):
+    """Rows of up to 7 blocks, every k: the chosen set is the only subset of
+    size min(k, n) whose every member beats every non-member (higher score,
+    or an equal score at a lower index), found by trying all subsets."""
+    import itertools
+    rng = np.random.default_rng(63)
+    for trial in range(60):
+        n = int(rng.integers(0, 8))
+        row = rng.integers(-3, 4, size=max(n, 1)).astype(np.float32) + 0.5   # ties, no zeros
+        for k in range(1, 9):
+            got, _ = o.select_blocks(row.reshape(1, -1), _sel_positions([n]), kv_len=64, k=k)
+            m = min(k, n)
+
+            def beats(a, b):
+                return row[a] > row[b] or (row[a] == row[b] and a < b)
+            winners = [S for S in itertools.combinations(range(n), m)
+                       if all(beats(a, b) for a in S for b in range(n) if b not in S)]
+            assert len(winners) == 1, (n, k, winners)
+            want = list(winners[0]) + [-1] * (k - m)
+            assert got[0].tolist() == want, (trial, n, k, row.tolist(), got[0].tolist())
+
+
 ALL_PINS = [
     pin_f16_decode, pin_f16_encode, pin_e4m3_library, pin_e4m3_landmarks, pin_quantizer_nearest,
     pin_decode_dense, pin_decode_fp16_rounding, pin_decode_convex, pin_decode_page_permutation,
@@ -420,4 +527,6 @@ ALL_PINS = [
     pin_decode_split_merge, pin_decode_inert, pin_gather_rows,
     pin_prefill_dense, pin_prefill_all_blocks_is_causal, pin_prefill_equals_decode_on_gathered,
     pin_prefill_token_lists, pin_prefill_inert,
+    pin_select_library, pin_select_closed_forms, pin_select_total_order, pin_select_inert,
+    pin_select_brute_force,
 ]

@@ -40,6 +40,17 @@ MUTANTS = {
     "kv_scale_dropped": ("return orc_e4m3_to_f64(((const uint8_t*)p->base)[off]) * p->scale;",
                          "return orc_e4m3_to_f64(((const uint8_t*)p->base)[off]);"),
     "normaliser_off_by_one": ("double w = x[i] / l;", "double w = x[i] / (l + 1e-3);"),
+    "select_ties_to_higher_index": ("return (a->idx > b->idx) - (a->idx < b->idx);",
+                                    "return (a->idx < b->idx) - (a->idx > b->idx);"),
+    "select_negatives_not_reversed": ("return a > b ? -1 : 1;\n}", "return a < b ? -1 : 1;\n}"),
+    "select_sign_flipped": ("return neg_a ? -1 : 1;", "return neg_a ? 1 : -1;"),
+    "select_includes_own_block": ("int64_t n = p / 4;", "int64_t n = p / 4 + 1;"),
+    "select_keeps_k_minus_1": ("const int64_t m = n < k ? n : k;",
+                               "const int64_t m = n < k ? n : k - 1;"),
+    "select_unsorted_output": ("qsort(pick, (size_t)m, sizeof(int32_t), orc_int32_ascending);",
+                               ";"),
+    "select_no_qpos_clamp": ("fl |= ORC_FLAG_QPOS_CLAMPED;\n            p = kv_len - 1;",
+                             "fl |= ORC_FLAG_QPOS_CLAMPED;\n            p = p;"),
     "bad_page_kept": ("if (page < 0 || page >= num_pages)\n        return -1;",
                       "if (page < 0 || page > num_pages)\n        return -1;"),
 }
