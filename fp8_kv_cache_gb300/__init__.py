@@ -43,6 +43,7 @@ FLAG_SEQ_CLAMPED = 2
 FLAG_EMPTY_ROW = 4
 FLAG_QPOS_CLAMPED = 8
 FLAG_BAD_SEL = 16
+FLAG_SCORES_SHORT = 32
 
 
 class PagedGQAError(RuntimeError):
@@ -104,6 +105,8 @@ def lib():
             L.paged_gqa_sparse_prefill_tokens.argtypes = [vp, i32, i32, vp, i32, vp, i32, i32,
                                                           vp, vp]
             L.paged_gqa_sparse_prefill_tokens.restype = i32
+            L.paged_gqa_select_blocks.argtypes = [vp, i64, i32, vp, i32, i32, i32, vp, vp, vp]
+            L.paged_gqa_select_blocks.restype = i32
             _lib = L
     return _lib
 
@@ -285,4 +288,24 @@ def paged_gqa_sparse_prefill_tokens(block_table, num_pages, kv_len, sel_idx, q_p
         _ptr(block_table), num_pages, kv_len, _ptr(sel_idx) if n_sel else None, n_sel,
         _ptr(q_pos), R, page_size, _ptr(out), _stream(stream))
     _check(st, "paged_gqa_sparse_prefill_tokens")
+    return out
+
+
+def paged_gqa_select_blocks(scores, q_pos, kv_len, k, *, n_blocks=None, out=None, err_flag=None,
+                            stream=None):
+    """QSA block selection: for each row the min(k, n) best of its causal
+    blocks by score (ties to the lower index), ascending, padded with -1.
+    scores float32 [R, >= n_blocks] on the GPU (unit column stride, any row
+    stride); q_pos int32 [R].  Returns int32 [R, k]."""
+    torch = _torch()
+    if scores.dtype != torch.float32 or scores.dim() != 2 or scores.stride(1) != 1:
+        raise ValueError("scores must be a 2-D float32 tensor with unit column stride")
+    R = scores.shape[0]
+    n_blocks = scores.shape[1] if n_blocks is None else int(n_blocks)
+    if out is None:
+        out = torch.empty((R, int(k)), dtype=torch.int32, device=scores.device)
+    st = lib().paged_gqa_select_blocks(_ptr(scores), scores.stride(0), n_blocks, _ptr(q_pos), R,
+                                       int(kv_len), int(k), _ptr(out), _ptr(err_flag),
+                                       _stream(stream))
+    _check(st, "paged_gqa_select_blocks")
     return out

@@ -309,4 +309,29 @@ int paged_gqa_sparse_prefill_tokens(const int32_t* block_table, int num_pages, i
     return e == cudaSuccess ? PAGED_GQA_OK : PAGED_GQA_ERR_CUDA;
 }
 
+int paged_gqa_select_blocks(const float* scores, int64_t score_stride, int n_blocks,
+                            const int32_t* q_pos, int R, int kv_len, int k,
+                            int32_t* sel_out, int* err_flag, void* stream)
+{
+    if (R < 0 || k < 0 || n_blocks < 0 || score_stride < n_blocks)
+        return PAGED_GQA_ERR_SHAPE;
+    if (q_pos == nullptr || (k > 0 && sel_out == nullptr) || (n_blocks > 0 && scores == nullptr))
+        return PAGED_GQA_ERR_NULL_POINTER;
+    if (R == 0 || k == 0)
+        return PAGED_GQA_OK;
+    SelectArgs a{};
+    a.scores = scores;
+    a.stride = score_stride;
+    a.n_blocks = n_blocks;
+    a.q_pos = q_pos;
+    a.R = R;
+    a.kv_len = kv_len;
+    a.k = k;
+    a.stage_keys = select_stage_keys(n_blocks);
+    a.out = sel_out;
+    a.err = err_flag;
+    const cudaError_t e = launch_select(a, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PAGED_GQA_OK : PAGED_GQA_ERR_CUDA;
+}
+
 }  // extern "C"

@@ -54,6 +54,17 @@ struct PrefillArgs {
     int* err;
 };
 
+struct SelectArgs {
+    const float* scores;
+    int64_t stride;
+    int n_blocks;
+    const int32_t* q_pos;
+    int R, kv_len, k;
+    int stage_keys;      // keys a CTA stages in shared memory (select_stage_keys)
+    int32_t* out;
+    int* err;
+};
+
 size_t decode_split_smem(bool e4m3, int B);
 size_t workspace_bytes(int B, int Hkv, int C);
 int split_ctas_per_sm(bool e4m3);
@@ -63,6 +74,8 @@ cudaError_t launch_prefill(const PrefillArgs& a, bool e4m3, cudaStream_t s);
 cudaError_t launch_gather(const KVGeom& g, bool e4m3, const int32_t* bt, int64_t bt_stride,
                           const int32_t* seq_lens, int B, int T, int Hkv, int max_seq_len,
                           float kv_scale, float* out, cudaStream_t s);
+int select_stage_keys(int n_blocks);
+cudaError_t launch_select(const SelectArgs& a, cudaStream_t s);
 cudaError_t launch_prefill_tokens(const KVGeom& g, const int32_t* bt, int kv_len,
                                   const int32_t* sel, int n_sel, const int32_t* q_pos, int R,
                                   int32_t* out, cudaStream_t s);

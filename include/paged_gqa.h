@@ -72,6 +72,7 @@ typedef enum {
 #define PAGED_GQA_FLAG_EMPTY_ROW    4  /* seq_len <= 0 or q_pos < 0: that output row is zero         */
 #define PAGED_GQA_FLAG_QPOS_CLAMPED 8  /* q_pos >= kv_len: clamped to kv_len - 1                     */
 #define PAGED_GQA_FLAG_BAD_SEL     16  /* selected block at or after the row's own block: skipped   */
+#define PAGED_GQA_FLAG_SCORES_SHORT 32  /* a selection row has more causal blocks than scores given  */
 
 typedef enum {
     PAGED_GQA_KV_FP16 = 0,            /* binary16 K/V                            */
@@ -206,6 +207,35 @@ int paged_gqa_sparse_prefill(const void* q, const void* k_cache, const void* v_c
                              int R, int Hq, int Hkv, int D, int page_size,
                              float kv_scale, float softmax_scale,
                              void* out, int* err_flag, void* stream);
+
+/*
+ * QSA block selection ("[Kernel][SM70] Accelerate exact Qwen3.8 decode",
+ * Implementation: radix selection over the block scores, ties at the pivot
+ * taken by increasing block index), producing the sel_idx rows that
+ * paged_gqa_sparse_prefill consumes.  For query row r with
+ * p = min(q_pos[r], kv_len - 1), the candidates are the blocks before the
+ * row's own block, i = 0 .. n - 1 with n = min(p / 4, n_blocks), scored
+ * scores[r * score_stride + i].  The row's output is the min(k, n) best
+ * candidates -- greater score first under IEEE 754 totalOrder (-NaN < -inf
+ * < ... < -0 < +0 < ... < +inf < +NaN), equal scores by increasing index --
+ * listed in increasing index order, then -1 up to k entries.  The result is
+ * exact (integer work on the scores' bit patterns) and deterministic.
+ *
+ *  scores        device float32; row r starts at scores + r * score_stride
+ *                (score_stride >= n_blocks, in elements).
+ *  n_blocks      scores per row; a row with p / 4 > n_blocks uses the first
+ *                n_blocks (PAGED_GQA_FLAG_SCORES_SHORT).
+ *  q_pos         device int32 [R]; q_pos < 0 (or kv_len <= 0) gives a row of
+ *                -1 (PAGED_GQA_FLAG_EMPTY_ROW); q_pos >= kv_len is clamped
+ *                (PAGED_GQA_FLAG_QPOS_CLAMPED).
+ *  k             selected blocks per row (>= 0).
+ *  sel_out       device int32 [R, k]; fully written.
+ *  err_flag      optional device int receiving PAGED_GQA_FLAG_* bits.
+ * One kernel is launched; nothing is allocated.
+ */
+int paged_gqa_select_blocks(const float* scores, int64_t score_stride, int n_blocks,
+                            const int32_t* q_pos, int R, int kv_len, int k,
+                            int32_t* sel_out, int* err_flag, void* stream);
 
 /*
  * Inspection: the rows the decode kernels gather, dequantised.  For every

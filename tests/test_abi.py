@@ -33,7 +33,7 @@ def test_header_declares_entry_points():
     names = _header_functions()
     for n in ("paged_gqa_decode", "paged_gqa_sparse_prefill", "paged_gqa_decode_workspace_size",
               "paged_gqa_gather_dequant", "paged_gqa_sparse_prefill_tokens",
-              "paged_gqa_status_string", "paged_gqa_version"):
+              "paged_gqa_select_blocks", "paged_gqa_status_string", "paged_gqa_version"):
         assert n in names
 
 
@@ -56,11 +56,12 @@ def test_flag_bits_match_header_and_oracle():
     bits = {m.group(1): int(m.group(2))
             for m in re.finditer(r"#define PAGED_GQA_FLAG_(\w+)\s+(\d+)", text)}
     assert bits == {"BAD_PAGE": 1, "SEQ_CLAMPED": 2, "EMPTY_ROW": 4, "QPOS_CLAMPED": 8,
-                    "BAD_SEL": 16}
+                    "BAD_SEL": 16, "SCORES_SHORT": 32}
     assert (oracle.FLAG_BAD_PAGE, oracle.FLAG_SEQ_CLAMPED, oracle.FLAG_EMPTY_ROW,
             oracle.FLAG_QPOS_CLAMPED, oracle.FLAG_BAD_SEL) == (1, 2, 4, 8, 16)
     assert (P.FLAG_BAD_PAGE, P.FLAG_SEQ_CLAMPED, P.FLAG_EMPTY_ROW, P.FLAG_QPOS_CLAMPED,
             P.FLAG_BAD_SEL) == (1, 2, 4, 8, 16)
+    assert oracle.FLAG_SCORES_SHORT == P.FLAG_SCORES_SHORT == 32
 
 
 A = 0x10000   # a fake, 16-byte aligned, non-NULL address (never dereferenced)
@@ -165,6 +166,19 @@ def test_inspection_entry_points_validate(L):
     assert L.paged_gqa_sparse_prefill_tokens(A, 8, 64, A, 4, A, 3, 6, A, None) == -3
     assert L.paged_gqa_sparse_prefill_tokens(None, 8, 64, A, 4, A, 3, 16, A, None) == -1
     assert L.paged_gqa_sparse_prefill_tokens(A, 8, 64, A, 4, A, 0, 16, A, None) == 0
+
+
+@host_only
+def test_select_blocks_validates(L):
+    # (scores, score_stride, n_blocks, q_pos, R, kv_len, k, sel_out, err_flag, stream)
+    assert L.paged_gqa_select_blocks(A, 8, 16, A, 4, 64, 4, A, None, None) == -3   # stride < n
+    assert L.paged_gqa_select_blocks(A, 16, 16, A, -1, 64, 4, A, None, None) == -3
+    assert L.paged_gqa_select_blocks(A, 16, 16, A, 4, 64, -2, A, None, None) == -3
+    assert L.paged_gqa_select_blocks(None, 16, 16, A, 4, 64, 4, A, None, None) == -1
+    assert L.paged_gqa_select_blocks(A, 16, 16, None, 4, 64, 4, A, None, None) == -1
+    assert L.paged_gqa_select_blocks(A, 16, 16, A, 4, 64, 4, None, None, None) == -1
+    assert L.paged_gqa_select_blocks(A, 16, 16, A, 0, 64, 4, A, None, None) == 0
+    assert L.paged_gqa_select_blocks(A, 16, 16, A, 4, 64, 0, None, None, None) == 0
 
 
 def test_workspace_size_for_forced_splits(L):
