@@ -16,7 +16,9 @@ step (~470 MB) exceed L2 as well.
 
 The same line reports the selected-sparse prefill (4096 rows, 512 selected
 four-token blocks + a 1..3-token tail, Hq6/Hkv1/D256 FP16, interleaved K/V,
-32768-token cache) timed the same way, the roofline of the dominant kernel
+32768-token cache) timed the same way, the same prefill over an E4M3 copy of
+the cache, the QSA block selection that produces such selections (4096 rows
+of 8192 block scores, k = 512), the roofline of the dominant kernel
 (the decode split kernel, timed by CUDA events the library records around it
 on the launching stream), an end-to-end number through host buffers, SM
 clocks sampled during the timed phases, and the FP64 CPU oracle timed on a
@@ -188,6 +190,8 @@ def run_ours(args, rank, world):
 
     if args.phase == "prefill":
         return run_prefill_only(args, dev)
+    if args.phase == "select":
+        return run_select_only(args, dev)
     case = W.long_e4m3()
     kvb = decode_kv_bytes(case)
     kv = torch.from_numpy(case.kv).to(dev)
@@ -299,40 +303,57 @@ def run_ours(args, rank, world):
     assert torch.equal(out_h, out.cpu()), "end-to-end output differs from the device result"
     e2e_value = world * kvb * Ke / (e_ms * 1e-3) / 1e9
 
-    # ---- selected-sparse prefill, 4096 rows
-    pc = W.sparse_prefill_4096()
-    pkv = torch.from_numpy(pc.kv).to(dev)
-    pk, pv = pkv[:, :, :, 0, :], pkv[:, :, :, 1, :]
-    pq = torch.from_numpy(pc.q).to(dev)
-    pbt = torch.from_numpy(pc.block_table).to(dev)
-    psel = torch.from_numpy(pc.sel_idx).to(dev)
-    ppos = torch.from_numpy(pc.q_pos).to(dev)
-    pout = torch.empty_like(pq)
-
-    def prefill():
-        P.paged_gqa_sparse_prefill(pq, pk, pv, pbt, pc.kv_len, psel, ppos, pc.page_size,
-                                   pc.softmax_scale, pc.kv_scale, pout)
-
     Kp = max(1, min(K, 50))
-    for _ in range(max(3, Wm)):
-        prefill()
-        flush_l2()
-    torch.cuda.synchronize()
-    p_ms = 0.0
-    for _ in range(Kp):
-        a, b = mk(), mk()
-        a.record()
-        prefill()
-        b.record()
-        flush_l2()
+
+    def time_phase(fn):
+        """Mean ms of Kp launches of fn, each between L2 flushes."""
+        for _ in range(max(3, Wm)):
+            fn()
+            flush_l2()
         torch.cuda.synchronize()
-        p_ms += a.elapsed_time(b)
+        total = 0.0
+        for _ in range(Kp):
+            a, b = mk(), mk()
+            a.record()
+            fn()
+            b.record()
+            flush_l2()
+            torch.cuda.synchronize()
+            total += a.elapsed_time(b)
+        return total / Kp
+
+    # ---- selected-sparse prefill, 4096 rows, FP16 and E4M3 caches
+    def prefill_phase(kv_dtype):
+        pc = W.sparse_prefill_4096(kv_dtype=kv_dtype)
+        pkv = torch.from_numpy(pc.kv).to(dev)
+        pk, pv = pkv[:, :, :, 0, :], pkv[:, :, :, 1, :]
+        pq = torch.from_numpy(pc.q).to(dev)
+        pbt = torch.from_numpy(pc.block_table).to(dev)
+        psel = torch.from_numpy(pc.sel_idx).to(dev)
+        ppos = torch.from_numpy(pc.q_pos).to(dev)
+        pout = torch.empty_like(pq)
+        ms = time_phase(lambda: P.paged_gqa_sparse_prefill(
+            pq, pk, pv, pbt, pc.kv_len, psel, ppos, pc.page_size, pc.softmax_scale,
+            pc.kv_scale, pout))
+        toks = prefill_tokens(pc)
+        gathered = toks * pc.Hkv * 2 * pc.D * pc.kv.itemsize
+        flops = 4.0 * toks * pc.Hq * pc.D      # QK^T and PV, 2 flops per multiply-add
+        return pc, ms, toks, gathered, flops
+
+    pc, p_ms, toks, gathered, flops = prefill_phase("fp16")
+    pc8, p8_ms, toks8, gathered8, _ = prefill_phase("e4m3")
+
+    # ---- QSA block selection: 4096 rows of 8192 block scores, k = 512
+    sc = W.qsa_select_4096()
+    s_scores = torch.from_numpy(sc.scores).to(dev)
+    s_qpos = torch.from_numpy(sc.q_pos).to(dev)
+    s_out = torch.empty((sc.scores.shape[0], sc.k), dtype=torch.int32, device=dev)
+    s_ms = time_phase(lambda: P.paged_gqa_select_blocks(s_scores, s_qpos, sc.kv_len, sc.k,
+                                                        out=s_out))
     clocks.stop()
-    p_ms /= Kp
-    toks = prefill_tokens(pc)
-    row_bytes = pc.D * pc.kv.itemsize
-    gathered = toks * pc.Hkv * 2 * row_bytes
-    flops = 4.0 * toks * pc.Hq * pc.D      # QK^T and PV, 2 flops per multiply-add
+    s_rows = sc.scores.shape[0]
+    s_cands = int(np.minimum(sc.q_pos.astype(np.int64) // 4, sc.n_blocks).sum())
+    s_bytes = 4 * s_cands + 4 * s_rows * sc.k + 4 * s_rows     # scores read, sel written, q_pos
 
     peak, peak_kind = measured_peaks()
     split_avg = float(np.mean(split_ms))
@@ -382,6 +403,19 @@ def run_ours(args, rank, world):
             "tflops": round(flops / (p_ms * 1e-3) / 1e12, 2),
             "pages_context_ms_v100": 8.84736,
         },
+        "sparse_prefill_e4m3": {
+            "workload": "the same 4096 rows over an E4M3 copy of the cache (per-tensor scale)",
+            "ms": round(p8_ms, 4), "rows_per_s": round(world * pc8.R / (p8_ms * 1e-3), 1),
+            "gathered_GBps": round(gathered8 / (p8_ms * 1e-3) / 1e9, 1),
+        },
+        "qsa_select": {
+            "workload": "4096 rows of 8192 block scores (row r ranks the 4096 + r blocks before "
+                        "its own), k = 512, bfloat16-precision N(0,1) scores",
+            "ms": round(s_ms, 4), "rows_per_s": round(world * s_rows / (s_ms * 1e-3), 1),
+            "algorithmic_bytes": s_bytes,
+            "GBps": round(s_bytes / (s_ms * 1e-3) / 1e9, 1),
+            "hbm_frac": round(s_bytes / (s_ms * 1e-3) / 1e9 / peak, 4),
+        },
         "gpu_launches": 2 * K,
         "clocks": clocks.summary(),
         "wall_s_timed_decode": round(wall, 4),
@@ -413,6 +447,27 @@ def run_prefill_only(args, dev):
         if i >= args.warmup:
             ms.append(a.elapsed_time(b))
     return {"phase": "prefill", "ms": float(np.mean(ms))}
+
+
+def run_select_only(args, dev):
+    """The QSA selection phase alone (for profiling)."""
+    import torch
+    import fp8_kv_cache_gb300 as P
+    from fp8_kv_cache_gb300 import workloads as W
+    sc = W.qsa_select_4096()
+    s_scores = torch.from_numpy(sc.scores).to(dev)
+    s_qpos = torch.from_numpy(sc.q_pos).to(dev)
+    s_out = torch.empty((sc.scores.shape[0], sc.k), dtype=torch.int32, device=dev)
+    ms = []
+    for i in range(args.warmup + args.steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        P.paged_gqa_select_blocks(s_scores, s_qpos, sc.kv_len, sc.k, out=s_out)
+        b.record()
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            ms.append(a.elapsed_time(b))
+    return {"phase": "select", "ms": float(np.mean(ms))}
 
 
 def cpu_baseline(sample_seqs=4, threads=None):
@@ -483,7 +538,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--phase", choices=["all", "decode", "prefill"], default="all",
+    ap.add_argument("--phase", choices=["all", "decode", "prefill", "select"], default="all",
                     help="run only one phase (for profiling); the JSON line needs 'all'")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -260,12 +260,14 @@ def prefill_case(name, *, R, n_sel, seed, first_block, Hq=6, Hkv=1, D=256, page_
                        interleaved=interleaved)
 
 
-def sparse_prefill_4096(seed=5, interleaved=True, R=4096):
-    """4096 rows, Hq6/Hkv1/D256 FP16, a 32768-token cache in 2048 shuffled
-    pages of 16; row r owns block 4096 + r (positions >= 16384 > 2051) and
-    attends to 512 selected blocks plus a tail of 1..3 tokens."""
-    return prefill_case(f"sparse_prefill_r{R}", R=R, n_sel=512, seed=seed, first_block=4096,
-                        kv_len=32768, interleaved=interleaved)
+def sparse_prefill_4096(seed=5, interleaved=True, R=4096, kv_dtype="fp16"):
+    """4096 rows, Hq6/Hkv1/D256 FP16 (or E4M3 KV with a per-tensor scale), a
+    32768-token cache in 2048 shuffled pages of 16; row r owns block 4096 + r
+    (positions >= 16384 > 2051) and attends to 512 selected blocks plus a tail
+    of 1..3 tokens."""
+    suffix = "" if kv_dtype == "fp16" else f"_{kv_dtype}"
+    return prefill_case(f"sparse_prefill_r{R}{suffix}", R=R, n_sel=512, seed=seed,
+                        first_block=4096, kv_len=32768, interleaved=interleaved, kv_dtype=kv_dtype)
 
 
 @dataclass

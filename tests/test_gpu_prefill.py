@@ -81,6 +81,17 @@ def test_full_4096_rows_sampled():
     assert np.array_equal(got.view(np.uint16), again.view(np.uint16)), "run-to-run"
 
 
+def test_full_4096_rows_interleaved_e4m3_sampled():
+    """The E4M3 prefill exactly as the benchmark times it."""
+    c = W.sparse_prefill_4096(kv_dtype="e4m3")
+    got, flags = U.run_prefill(c)
+    rows = np.random.default_rng(9).choice(c.R, size=24, replace=False).astype(np.int32)
+    rows = np.concatenate([rows, [0, c.R - 1]]).astype(np.int32)
+    want, _, oflags = U.oracle_prefill(c, rows=rows)
+    U.assert_close(got[rows], want[rows], c.name)
+    assert flags == 0 and oflags == 0
+
+
 def test_full_4096_rows_contiguous_e4m3_sampled():
     c = W.prefill_case("prefill_4096_e4m3", R=4096, n_sel=512, seed=6, first_block=4096,
                        kv_len=32768, interleaved=False, kv_dtype="e4m3")
