@@ -15,6 +15,11 @@ Shapes and value distributions follow the workloads the pages describe:
   selected four-token blocks plus a causal tail of 1..3 tokens, contiguous or
   interleaved K/V ("[Kernel][SM70] Accelerate Qwen3.8 QSA paged prefill",
   Changes and Test Result);
+* top-k/top-p masking: float32 logits of B8/B16 x 248,320 ("[Kernel][SM70]
+  Scale NVFP4 E4M3 decode batches", Purpose; top-k 20, top-p 0.95 from its
+  Performance contract).  No trained model is at hand: each row is
+  N(0, 2.5^2) with 32 positions raised by U(5, 15), so a handful of logits
+  carry most of the mass, as in a language model's next-token distribution;
 * block selection: float32 block scores of the same 4096 rows, from which 512
   blocks per row are selected ("[Kernel][SM70] Accelerate exact Qwen3.8
   decode", Implementation).  The pages' scores come from a trained scorer,
@@ -310,3 +315,28 @@ def qsa_select_4096(seed=6, R=4096):
     before each row's own, from bfloat16-precision N(0,1) scores."""
     return select_case(f"qsa_select_r{R}", R=R, n_blocks=8192, k=512, seed=seed, kv_len=32768,
                        first_block=4096)
+
+
+@dataclass
+class MaskCase:
+    """Inputs of one top-k/top-p masking call: logits float32 [B, V]."""
+    name: str
+    logits: np.ndarray
+    k: int
+    p: float
+
+
+def logits_case(name, *, B, V=248320, k=20, p=0.95, seed=7, peaks=32):
+    """B rows of V logits: N(0, 2.5^2) plus U(5, 15) at ``peaks`` random
+    positions per row."""
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((B, V)).astype(np.float32) * np.float32(2.5)
+    for b in range(B):
+        idx = rng.choice(V, size=min(peaks, V), replace=False)
+        x[b, idx] += rng.uniform(5.0, 15.0, size=idx.size).astype(np.float32)
+    return MaskCase(name=name, logits=x, k=int(k), p=float(p))
+
+
+def sampler_b16(seed=7):
+    """B=16 rows of 248,320 logits, top-k 20, top-p 0.95."""
+    return logits_case("topk_topp_b16", B=16, seed=seed)

@@ -12,7 +12,9 @@ follows (1Cat-vLLM pull requests):
 * sparse prefill and the inert-input rules: "[Kernel][SM70] Accelerate Qwen3.8
   QSA paged prefill" (#378), Changes;
 * QSA block selection (top-k of block scores, ties to the lower index):
-  "[Kernel][SM70] Accelerate exact Qwen3.8 decode" (#415), Implementation.
+  "[Kernel][SM70] Accelerate exact Qwen3.8 decode" (#415), Implementation;
+* the combined top-k/top-p masking of the decode step's logits: "[Kernel]
+  [SM70] Scale NVFP4 E4M3 decode batches" (#282), Purpose.
 
 ``Oracle(path)`` loads any compiled copy of the source (the tests use this to
 check that deliberately broken copies fail the pins); the module-level
@@ -116,6 +118,8 @@ class Oracle:
         lib.orc_sparse_row_tokens.restype = i64
         lib.orc_select_blocks.argtypes = [vp, i64, i32, vp, i32, i32, i32, vp, vp, i32]
         lib.orc_select_blocks.restype = i32
+        lib.orc_topk_topp_mask.argtypes = [vp, i64, i32, i32, i32, dbl, vp, i64, vp, i32]
+        lib.orc_topk_topp_mask.restype = i32
         self.lib = lib
         self.path = path
 
@@ -222,6 +226,23 @@ class Oracle:
             raise ValueError("oracle rejected the selection shapes" if rc == -1 else "out of memory")
         return sel, flags.value
 
+    def topk_topp_mask(self, logits, k, p, threads=None):
+        """Combined top-k/top-p masking.  logits float32 [B, V] (unit column
+        stride).  Returns (masked float32 [B, V], margin float64 [B])."""
+        x = np.asarray(logits, dtype=np.float32)
+        if x.ndim != 2 or x.strides[1] != 4:
+            raise ValueError("logits must be 2-D float32 with unit column stride")
+        B, V = x.shape
+        out = np.empty((B, V), dtype=np.float32)
+        margin = np.empty(B, dtype=np.float64)
+        rc = self.lib.orc_topk_topp_mask(x.ctypes.data, x.strides[0] // 4, B, V, int(k),
+                                         float(np.float32(p)), out.ctypes.data, V,
+                                         margin.ctypes.data, threads or default_threads())
+        if rc != 0:
+            raise ValueError({-1: "bad arguments", -2: "out of memory",
+                              -3: "NaN or +inf logit"}.get(rc, str(rc)))
+        return out, margin
+
     def gather_rows(self, cache, block_table, seq_lens, page_size, num_pages, max_seq_len,
                     kv_scale=1.0, T=None, threads=None):
         """Gathered, dequantised rows [B, T, Hkv, D] float32 of one K or V pool
@@ -273,3 +294,7 @@ def gather_rows(*args, **kwargs):
 
 def select_blocks(*args, **kwargs):
     return default().select_blocks(*args, **kwargs)
+
+
+def topk_topp_mask(*args, **kwargs):
+    return default().topk_topp_mask(*args, **kwargs)

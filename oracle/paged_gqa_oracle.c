@@ -18,6 +18,10 @@
  *       last; block tables in physical-page units; contiguous or interleaved
  *       K/V strides; padded or stale positions clamped to the live length and
  *       invalid requests made inert.
+ *   [D] also lists, as the decode step's second operator, the combined
+ *       top-k/top-p masking of B8/B16 x 248,320 logits (Purpose; run with
+ *       top-k 20, top-p 0.95 in the Performance contract; compared bitwise
+ *       against its rollback in Test plan and result).
  *   [S] "[Kernel][SM70] Accelerate exact Qwen3.8 decode" (#415),
  *       Implementation and Focused tests: QSA's block selection, a radix
  *       selection over the block scores whose ties at the pivot go to the
@@ -564,4 +568,112 @@ int orc_select_blocks(const float* scores, int64_t score_stride, int n_blocks,
     if (flags != NULL)
         *flags |= fl;
     return oom ? -2 : 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Combined top-k / top-p masking [D]                                          */
+/* ------------------------------------------------------------------------- */
+/*
+ * For each row of V logits: top-k keeps the min(k, V) largest logits (equal
+ * logits: the lower index first, the tie rule of [S]); top-p then keeps, of
+ * those in that order, the shortest leading run whose probability mass
+ * reaches p, the probabilities being the softmax over the top-k logits; every
+ * logit not kept becomes -infinity, kept logits pass through unchanged.
+ *
+ * Readings taken where the pages are silent (listed in the design doc):
+ *   - top-k keeps exactly min(k, V) logits, ties to the lower index;
+ *   - the top-p mass is computed in FP64: e_j = exp(x_j - x_0) over the
+ *     top-k list in order (x_0 its largest), suffix sums S_j = e_j + S_{j+1}
+ *     accumulated from the end of the list, Z = S_0; logit j is kept iff
+ *     S_j > (1 - p) Z, i.e. iff the mass of the logits before it is < p Z;
+ *   - a row whose largest logit is -infinity keeps its top-k list as is;
+ *   - logits are finite or -infinity (NaN and +infinity are outside the
+ *     contract and rejected here).
+ * margin (optional, [B]) receives min_j |S_j - (1 - p) Z| / Z: how far the
+ * row's top-p decisions are from their threshold.
+ */
+
+typedef struct {
+    float x;
+    int32_t idx;
+} orc_logit;
+
+/* Descending value, equal values by increasing index. */
+static int orc_logit_desc(const void* a_, const void* b_)
+{
+    const orc_logit* a = (const orc_logit*)a_;
+    const orc_logit* b = (const orc_logit*)b_;
+    if (a->x != b->x)
+        return a->x > b->x ? -1 : 1;
+    return (a->idx > b->idx) - (a->idx < b->idx);
+}
+
+/* Returns 0, -1 on bad arguments, -2 when memory runs out, -3 on a NaN or
+ * +infinity logit. */
+int orc_topk_topp_mask(const float* logits, int64_t stride, int B, int V, int k, double p,
+                       float* out, int64_t out_stride, double* margin, int n_threads)
+{
+    if (B < 0 || V < 1 || k < 1 || stride < V || out_stride < V || !(p > 0.0 && p <= 1.0))
+        return -1;
+    int bad = 0;
+#pragma omp parallel for num_threads(n_threads) schedule(dynamic, 1) reduction(|:bad)
+    for (int b = 0; b < B; ++b) {
+        const float* x = logits + (int64_t)b * stride;
+        float* o = out + (int64_t)b * out_stride;
+        orc_logit* l = (orc_logit*)malloc((size_t)V * sizeof(orc_logit));
+        if (l == NULL) {
+            bad |= 2;
+            continue;
+        }
+        int finite = 1;
+        for (int i = 0; i < V; ++i) {
+            if (isnan(x[i]) || (isinf(x[i]) && x[i] > 0))
+                finite = 0;
+            l[i].x = x[i];
+            l[i].idx = i;
+        }
+        if (!finite) {
+            free(l);
+            bad |= 4;
+            continue;
+        }
+        qsort(l, (size_t)V, sizeof(orc_logit), orc_logit_desc);
+        const int K = k < V ? k : V;
+        int m = K;
+        double mg = INFINITY;
+        if (l[0].x != -INFINITY) {
+            double* S = (double*)malloc((size_t)(K + 1) * sizeof(double));
+            if (S == NULL) {
+                free(l);
+                bad |= 2;
+                continue;
+            }
+            const double x0 = (double)l[0].x;
+            S[K] = 0.0;
+            for (int j = K - 1; j >= 0; --j)
+                S[j] = exp((double)l[j].x - x0) + S[j + 1];
+            const double Z = S[0], cut = (1.0 - p) * Z;
+            m = 0;
+            for (int j = 0; j < K; ++j) {
+                if (S[j] > cut)
+                    m = j + 1;
+                const double d = fabs(S[j] - cut) / Z;
+                if (d < mg)
+                    mg = d;
+            }
+            free(S);
+        }
+        for (int i = 0; i < V; ++i)
+            o[i] = -INFINITY;
+        for (int j = 0; j < m; ++j)
+            o[l[j].idx] = l[j].x;
+        if (margin != NULL)
+            margin[b] = mg;
+        free(l);
+    }
+    if (bad & 2)
+        return -2;
+    if (bad & 4)
+        return -3;
+    return 0;
 }

@@ -12,7 +12,11 @@ when it disagrees with:
   * for the block selection: numpy's stable argsort (ties to the lower index)
     on finite scores, closed forms (monotone and constant rows, k >= n), an
     IEEE totalOrder case written out by hand, the inert-row rules, and a
-    brute-force dominance check over every subset of tiny rows.
+    brute-force dominance check over every subset of tiny rows,
+  * for the top-k/top-p masking: numpy's stable argsort (top-k), the closed
+    forms of uniform and two-valued rows, the shortest-prefix formulation of
+    top-p through numpy's FP64 softmax and searchsorted, shift invariance at
+    large logits, and -inf logits carrying no mass.
 ``ALL_PINS`` runs them all; test_oracle.py runs each one on the committed
 oracle and test_oracle_mutants.py checks that broken copies fail some pin.
 """
@@ -520,6 +524,88 @@ def pin_select_brute_force(o):
             assert got[0].tolist() == want, (trial, n, k, row.tolist(), got[0].tolist())
 
 
+# ---------------------------------------------------------------- top-k / top-p masking
+
+def _kept(masked):
+    return [np.flatnonzero(r > -np.inf).tolist() for r in masked]
+
+
+def pin_mask_topk_library(o):
+    """p = 1: the kept logits are numpy's stable argsort of -x, first k
+    (equal logits keep increasing index order), values unchanged."""
+    rng = np.random.default_rng(71)
+    x = np.round(rng.standard_normal((6, 500)) * 8).astype(np.float32) / 4   # many ties
+    for k in (1, 7, 20, 499, 500, 800):
+        out, _ = o.topk_topp_mask(x, k, 1.0)
+        for r in range(x.shape[0]):
+            want = sorted(np.argsort(-x[r], kind="stable")[:k].tolist())
+            assert _kept(out[r:r + 1])[0] == want, (k, r)
+            assert np.array_equal(out[r, want], x[r, want])
+
+
+def pin_mask_uniform_rows(o):
+    """V equal logits, no top-k cut: every logit has mass 1/V, so top-p keeps
+    the first ceil(p V) indices.  Where p V is an integer and every mass is
+    exact in binary (V = 4, 8), the run of exactly p V logits already reaches
+    p and the next logit is not kept."""
+    x = np.full((1, 25), 0.75, dtype=np.float32)
+    for p, m in ((0.9, 23), (0.5, 13), (0.01, 1), (0.97, 25)):
+        out, _ = o.topk_topp_mask(x, 25, p)
+        assert _kept(out)[0] == list(range(m)), (p, _kept(out)[0])
+    for V, p, m in ((4, 0.5, 2), (8, 0.25, 2), (8, 0.75, 6), (4, 1.0, 4)):
+        out, _ = o.topk_topp_mask(np.full((1, V), -1.5, dtype=np.float32), V, p)
+        assert _kept(out)[0] == list(range(m)), (V, p, _kept(out)[0])
+
+
+def pin_mask_two_values(o):
+    """Logits 0 and ln 3 carry mass 1/4 and 3/4: p = 0.7 keeps ln 3 alone,
+    p = 0.8 keeps both; top-k 1 keeps ln 3 whatever p."""
+    x = np.array([[0.0, np.log(3.0)]], dtype=np.float32)
+    assert _kept(o.topk_topp_mask(x, 2, 0.7)[0])[0] == [1]
+    assert _kept(o.topk_topp_mask(x, 2, 0.8)[0])[0] == [0, 1]
+    assert _kept(o.topk_topp_mask(x, 1, 1.0)[0])[0] == [1]
+
+
+def pin_mask_topp_prefix(o):
+    """No top-k cut: the kept logits are the shortest run, in descending
+    order, whose cumulative probability reaches p (numpy FP64 softmax and
+    searchsorted), for rows whose decision is not within rounding of p."""
+    rng = np.random.default_rng(72)
+    x = (rng.standard_normal((12, 300)) * 2).astype(np.float32)
+    for p in (0.3, 0.9, 0.95):
+        out, margin = o.topk_topp_mask(x, 300, p)
+        for r in range(x.shape[0]):
+            if margin[r] < 1e-9:
+                continue
+            order = np.argsort(-x[r], kind="stable")
+            pr = np.exp(x[r, order].astype(np.float64) - float(x[r, order[0]]))
+            c = np.cumsum(pr / pr.sum())
+            m = int(np.searchsorted(c, p, side="left")) + 1
+            assert _kept(out[r:r + 1])[0] == sorted(order[:m].tolist()), (p, r)
+
+
+def pin_mask_shift_invariance(o):
+    """Adding 1024 to every logit (exact in binary32 for these values)
+    changes no decision: the softmax is shift-invariant, and exp must not
+    overflow."""
+    rng = np.random.default_rng(73)
+    x = (np.round(rng.standard_normal((8, 400)) * 64) / 64).astype(np.float32)
+    a, _ = o.topk_topp_mask(x, 30, 0.9)
+    b, _ = o.topk_topp_mask(x + np.float32(1024.0), 30, 0.9)
+    assert _kept(a) == _kept(b)
+
+
+def pin_mask_negative_infinity(o):
+    """-inf logits carry no mass: in a row of 3 finite logits and -infs,
+    k = 5 keeps at most the 3 finite ones; an all -inf row stays all -inf."""
+    x = np.full((2, 10), -np.inf, dtype=np.float32)
+    x[0, [2, 5, 7]] = [1.0, 3.0, 2.0]
+    out, _ = o.topk_topp_mask(x, 5, 1.0)
+    assert _kept(out)[0] == [2, 5, 7] and _kept(out)[1] == []
+    out, _ = o.topk_topp_mask(x, 5, 0.5)
+    assert _kept(out)[0] == [5]                 # 3.0 alone carries 0.665 >= 0.5
+
+
 ALL_PINS = [
     pin_f16_decode, pin_f16_encode, pin_e4m3_library, pin_e4m3_landmarks, pin_quantizer_nearest,
     pin_decode_dense, pin_decode_fp16_rounding, pin_decode_convex, pin_decode_page_permutation,
@@ -529,4 +615,6 @@ ALL_PINS = [
     pin_prefill_token_lists, pin_prefill_inert,
     pin_select_library, pin_select_closed_forms, pin_select_total_order, pin_select_inert,
     pin_select_brute_force,
+    pin_mask_topk_library, pin_mask_uniform_rows, pin_mask_two_values, pin_mask_topp_prefix,
+    pin_mask_shift_invariance, pin_mask_negative_infinity,
 ]

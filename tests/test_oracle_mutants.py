@@ -40,8 +40,8 @@ MUTANTS = {
     "kv_scale_dropped": ("return orc_e4m3_to_f64(((const uint8_t*)p->base)[off]) * p->scale;",
                          "return orc_e4m3_to_f64(((const uint8_t*)p->base)[off]);"),
     "normaliser_off_by_one": ("double w = x[i] / l;", "double w = x[i] / (l + 1e-3);"),
-    "select_ties_to_higher_index": ("return (a->idx > b->idx) - (a->idx < b->idx);",
-                                    "return (a->idx < b->idx) - (a->idx > b->idx);"),
+    "select_ties_to_higher_index": ("return -c;\n    return (a->idx > b->idx) - (a->idx < b->idx);",
+                                    "return -c;\n    return (a->idx < b->idx) - (a->idx > b->idx);"),
     "select_negatives_not_reversed": ("return a > b ? -1 : 1;\n}", "return a < b ? -1 : 1;\n}"),
     "select_sign_flipped": ("return neg_a ? -1 : 1;", "return neg_a ? 1 : -1;"),
     "select_includes_own_block": ("int64_t n = p / 4;", "int64_t n = p / 4 + 1;"),
@@ -51,6 +51,13 @@ MUTANTS = {
                                ";"),
     "select_no_qpos_clamp": ("fl |= ORC_FLAG_QPOS_CLAMPED;\n            p = kv_len - 1;",
                              "fl |= ORC_FLAG_QPOS_CLAMPED;\n            p = p;"),
+    "mask_ties_to_higher_index": ("return (a->idx > b->idx) - (a->idx < b->idx);\n}\n\n/* Returns 0, -1",
+                                  "return (a->idx < b->idx) - (a->idx > b->idx);\n}\n\n/* Returns 0, -1"),
+    "mask_keeps_at_threshold": ("if (S[j] > cut)", "if (S[j] >= cut)"),
+    "mask_cut_uses_p": ("cut = (1.0 - p) * Z;", "cut = p * Z;"),
+    "mask_ignores_topk": ("const int K = k < V ? k : V;", "const int K = V;"),
+    "mask_no_max_shift": ("const double x0 = (double)l[0].x;", "const double x0 = 0.0;"),
+    "mask_count_off_by_one": ("m = j + 1;", "m = j;"),
     "bad_page_kept": ("if (page < 0 || page >= num_pages)\n        return -1;",
                       "if (page < 0 || page > num_pages)\n        return -1;"),
 }
