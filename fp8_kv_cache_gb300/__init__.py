@@ -44,6 +44,7 @@ FLAG_EMPTY_ROW = 4
 FLAG_QPOS_CLAMPED = 8
 FLAG_BAD_SEL = 16
 FLAG_SCORES_SHORT = 32
+FLAG_BAD_LOGIT = 64
 
 
 class PagedGQAError(RuntimeError):
@@ -107,6 +108,8 @@ def lib():
             L.paged_gqa_sparse_prefill_tokens.restype = i32
             L.paged_gqa_select_blocks.argtypes = [vp, i64, i32, vp, i32, i32, i32, vp, vp, vp]
             L.paged_gqa_select_blocks.restype = i32
+            L.paged_gqa_topk_topp_mask.argtypes = [vp, i64, vp, i64, i32, i32, i32, f32, vp, vp]
+            L.paged_gqa_topk_topp_mask.restype = i32
             _lib = L
     return _lib
 
@@ -308,4 +311,22 @@ def paged_gqa_select_blocks(scores, q_pos, kv_len, k, *, n_blocks=None, out=None
                                        int(kv_len), int(k), _ptr(out), _ptr(err_flag),
                                        _stream(stream))
     _check(st, "paged_gqa_select_blocks")
+    return out
+
+
+def paged_gqa_topk_topp_mask(logits, k, p, *, out=None, err_flag=None, stream=None):
+    """Combined top-k/top-p masking: the kept logits unchanged, -inf
+    elsewhere.  logits float32 [B, V] on the GPU (unit column stride);
+    ``out=logits`` masks in place.  Returns out."""
+    torch = _torch()
+    if logits.dtype != torch.float32 or logits.dim() != 2 or logits.stride(1) != 1:
+        raise ValueError("logits must be a 2-D float32 tensor with unit column stride")
+    B, V = logits.shape
+    if out is None:
+        out = torch.empty_like(logits)
+    if out.shape != logits.shape or out.dtype != torch.float32 or out.stride(1) != 1:
+        raise ValueError("out must match logits")
+    st = lib().paged_gqa_topk_topp_mask(_ptr(logits), logits.stride(0), _ptr(out), out.stride(0),
+                                        B, V, int(k), float(p), _ptr(err_flag), _stream(stream))
+    _check(st, "paged_gqa_topk_topp_mask")
     return out

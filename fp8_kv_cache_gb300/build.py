@@ -20,7 +20,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(os.path.dirname(PKG), "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIBRARY = os.path.join(PKG, "libpaged_gqa.so")
-SOURCES = ["api.cu", "decode.cu", "prefill.cu", "inspect.cu", "select.cu", "decode_noalloc.cu"]
+SOURCES = ["api.cu", "decode.cu", "prefill.cu", "inspect.cu", "select.cu", "sample_mask.cu",
+           "decode_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -334,4 +334,33 @@ int paged_gqa_select_blocks(const float* scores, int64_t score_stride, int n_blo
     return e == cudaSuccess ? PAGED_GQA_OK : PAGED_GQA_ERR_CUDA;
 }
 
+int paged_gqa_topk_topp_mask(const float* logits, int64_t logits_stride, float* out,
+                             int64_t out_stride, int B, int V, int k, float p, int* err_flag,
+                             void* stream)
+{
+    if (B < 0 || V < 1 || logits_stride < V || out_stride < V || !(p > 0.f && p <= 1.f))
+        return PAGED_GQA_ERR_SHAPE;
+    if (!mask_supported(V, k))
+        return k < 1 ? PAGED_GQA_ERR_SHAPE : PAGED_GQA_ERR_UNSUPPORTED;
+    if (logits == nullptr || out == nullptr)
+        return PAGED_GQA_ERR_NULL_POINTER;
+    if (out == logits && out_stride != logits_stride)
+        return PAGED_GQA_ERR_SHAPE;
+    if (B == 0)
+        return PAGED_GQA_OK;
+    MaskArgs a{};
+    a.x = logits;
+    a.x_stride = logits_stride;
+    a.out = out;
+    a.out_stride = out_stride;
+    a.B = B;
+    a.V = V;
+    a.k = k;
+    a.slice = mask_slice(V);
+    a.p = p;
+    a.err = err_flag;
+    const cudaError_t e = launch_topk_topp(a, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PAGED_GQA_OK : PAGED_GQA_ERR_CUDA;
+}
+
 }  // extern "C"

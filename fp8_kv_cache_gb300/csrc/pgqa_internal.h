@@ -65,6 +65,17 @@ struct SelectArgs {
     int* err;
 };
 
+struct MaskArgs {
+    const float* x;
+    int64_t x_stride;
+    float* out;
+    int64_t out_stride;
+    int B, V, k;
+    int slice;           // columns per CTA of a row's cluster (mask_slice)
+    float p;
+    int* err;
+};
+
 size_t decode_split_smem(bool e4m3, int B);
 size_t workspace_bytes(int B, int Hkv, int C);
 int split_ctas_per_sm(bool e4m3);
@@ -75,6 +86,9 @@ cudaError_t launch_gather(const KVGeom& g, bool e4m3, const int32_t* bt, int64_t
                           const int32_t* seq_lens, int B, int T, int Hkv, int max_seq_len,
                           float kv_scale, float* out, cudaStream_t s);
 int select_stage_keys(int n_blocks);
+int mask_slice(int V);
+bool mask_supported(int V, int k);
+cudaError_t launch_topk_topp(const MaskArgs& a, cudaStream_t s);
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t s);
 cudaError_t launch_prefill_tokens(const KVGeom& g, const int32_t* bt, int kv_len,
                                   const int32_t* sel, int n_sel, const int32_t* q_pos, int R,

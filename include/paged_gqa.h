@@ -73,6 +73,7 @@ typedef enum {
 #define PAGED_GQA_FLAG_QPOS_CLAMPED 8  /* q_pos >= kv_len: clamped to kv_len - 1                     */
 #define PAGED_GQA_FLAG_BAD_SEL     16  /* selected block at or after the row's own block: skipped   */
 #define PAGED_GQA_FLAG_SCORES_SHORT 32  /* a selection row has more causal blocks than scores given  */
+#define PAGED_GQA_FLAG_BAD_LOGIT   64  /* a masking row's largest logit is NaN or +inf: top-p skipped */
 
 typedef enum {
     PAGED_GQA_KV_FP16 = 0,            /* binary16 K/V                            */
@@ -236,6 +237,34 @@ int paged_gqa_sparse_prefill(const void* q, const void* k_cache, const void* v_c
 int paged_gqa_select_blocks(const float* scores, int64_t score_stride, int n_blocks,
                             const int32_t* q_pos, int R, int kv_len, int k,
                             int32_t* sel_out, int* err_flag, void* stream);
+
+/*
+ * Combined top-k/top-p masking of the decode step's logits ("[Kernel][SM70]
+ * Scale NVFP4 E4M3 decode batches", Purpose: B8/B16 x 248,320 logits, run at
+ * top-k 20, top-p 0.95).  For each row of V logits: top-k keeps the min(k, V)
+ * largest (equal logits: the lower index first); top-p keeps, of those in
+ * that order, the shortest leading run whose probability mass reaches p, the
+ * probabilities being the softmax over the top-k logits, computed in FP64:
+ * e_j = exp(x_j - x_0), S_j = e_j + S_{j+1} summed from the end of the list,
+ * logit j kept iff S_j > (1 - p) S_0.  out = the kept logits, bit for bit,
+ * and -infinity everywhere else.
+ *
+ *  logits        device float32; row b starts at logits + b * logits_stride
+ *                (>= V, in elements).  Finite or -inf values; a row whose
+ *                largest logit is NaN or +inf keeps its top-k list
+ *                (PAGED_GQA_FLAG_BAD_LOGIT), a row of -inf stays -inf.
+ *  out           device float32, row stride out_stride (>= V); fully written.
+ *                out == logits (with equal strides) masks in place; any other
+ *                overlap is not allowed.
+ *  k             1 .. 128.
+ *  p             0 < p <= 1 (p = 1: top-k alone).
+ *  V             1 .. 327680.
+ *  err_flag      optional device int receiving PAGED_GQA_FLAG_* bits.
+ * One kernel is launched: a cluster of 8 CTAs per row; nothing is allocated.
+ */
+int paged_gqa_topk_topp_mask(const float* logits, int64_t logits_stride, float* out,
+                             int64_t out_stride, int B, int V, int k, float p, int* err_flag,
+                             void* stream);
 
 /*
  * Inspection: the rows the decode kernels gather, dequantised.  For every

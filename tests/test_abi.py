@@ -33,7 +33,8 @@ def test_header_declares_entry_points():
     names = _header_functions()
     for n in ("paged_gqa_decode", "paged_gqa_sparse_prefill", "paged_gqa_decode_workspace_size",
               "paged_gqa_gather_dequant", "paged_gqa_sparse_prefill_tokens",
-              "paged_gqa_select_blocks", "paged_gqa_status_string", "paged_gqa_version"):
+              "paged_gqa_select_blocks", "paged_gqa_topk_topp_mask", "paged_gqa_status_string",
+              "paged_gqa_version"):
         assert n in names
 
 
@@ -56,12 +57,13 @@ def test_flag_bits_match_header_and_oracle():
     bits = {m.group(1): int(m.group(2))
             for m in re.finditer(r"#define PAGED_GQA_FLAG_(\w+)\s+(\d+)", text)}
     assert bits == {"BAD_PAGE": 1, "SEQ_CLAMPED": 2, "EMPTY_ROW": 4, "QPOS_CLAMPED": 8,
-                    "BAD_SEL": 16, "SCORES_SHORT": 32}
+                    "BAD_SEL": 16, "SCORES_SHORT": 32, "BAD_LOGIT": 64}
     assert (oracle.FLAG_BAD_PAGE, oracle.FLAG_SEQ_CLAMPED, oracle.FLAG_EMPTY_ROW,
             oracle.FLAG_QPOS_CLAMPED, oracle.FLAG_BAD_SEL) == (1, 2, 4, 8, 16)
     assert (P.FLAG_BAD_PAGE, P.FLAG_SEQ_CLAMPED, P.FLAG_EMPTY_ROW, P.FLAG_QPOS_CLAMPED,
             P.FLAG_BAD_SEL) == (1, 2, 4, 8, 16)
     assert oracle.FLAG_SCORES_SHORT == P.FLAG_SCORES_SHORT == 32
+    assert P.FLAG_BAD_LOGIT == 64
 
 
 A = 0x10000   # a fake, 16-byte aligned, non-NULL address (never dereferenced)
@@ -179,6 +181,23 @@ def test_select_blocks_validates(L):
     assert L.paged_gqa_select_blocks(A, 16, 16, A, 4, 64, 4, None, None, None) == -1
     assert L.paged_gqa_select_blocks(A, 16, 16, A, 0, 64, 4, A, None, None) == 0
     assert L.paged_gqa_select_blocks(A, 16, 16, A, 4, 64, 0, None, None, None) == 0
+
+
+@host_only
+def test_topk_topp_mask_validates(L):
+    # (logits, logits_stride, out, out_stride, B, V, k, p, err_flag, stream)
+    ok = (A, 1000, A + 4096, 1000, 4, 1000, 20, 0.95)
+    assert L.paged_gqa_topk_topp_mask(None, *ok[1:], None, None) == -1
+    assert L.paged_gqa_topk_topp_mask(A, 1000, None, 1000, 4, 1000, 20, 0.95, None, None) == -1
+    assert L.paged_gqa_topk_topp_mask(A, 999, A + 4096, 1000, 4, 1000, 20, 0.95, None, None) == -3
+    assert L.paged_gqa_topk_topp_mask(A, 1000, A + 4096, 1000, -1, 1000, 20, 0.95, None, None) == -3
+    assert L.paged_gqa_topk_topp_mask(A, 1000, A + 4096, 1000, 4, 1000, 0, 0.95, None, None) == -3
+    assert L.paged_gqa_topk_topp_mask(A, 1000, A + 4096, 1000, 4, 1000, 129, 0.95, None, None) == -4
+    assert L.paged_gqa_topk_topp_mask(A, 400000, A, 400000, 4, 400000, 20, 0.95, None, None) == -4
+    for p in (0.0, -0.5, 1.5, float("nan")):
+        assert L.paged_gqa_topk_topp_mask(A, 1000, A + 4096, 1000, 4, 1000, 20, p, None, None) == -3
+    assert L.paged_gqa_topk_topp_mask(A, 1000, A, 1024, 4, 1000, 20, 0.95, None, None) == -3
+    assert L.paged_gqa_topk_topp_mask(A, 1000, A + 4096, 1000, 0, 1000, 20, 0.95, None, None) == 0
 
 
 def test_workspace_size_for_forced_splits(L):
