@@ -11,17 +11,23 @@
 // of the list, logit j kept iff S_j > (1 - p) S_0.
 //
 // Design (ours): one thread-block cluster of kMaskCtas CTAs per row, so a
-// handful of rows still spreads over the GPU.  Each CTA stages its slice of
-// the row (keys whose unsigned order is the numeric order of the logits) in
-// shared memory and finds the slice's own top-k with the radix selection of
-// select_core.cuh; the global top-k is among the union of those candidate
-// lists.  After a cluster barrier, rank 0 reads every CTA's candidates
-// through distributed shared memory (mapa + ld.shared::cluster), ranks them
-// (larger key first, equal keys by index), and runs the FP64 top-p over the
-// first min(k, V); after a second barrier every CTA reads the kept list from
-// rank 0 and writes its slice: -infinity everywhere except the kept logits,
-// which keep their bits.  A last barrier keeps rank 0's shared memory alive
-// until every CTA has read it.  HBM traffic: the row read once, written once.
+// handful of rows still spreads over the GPU.  Each CTA finds the top-k of
+// its slice of the row (keys whose unsigned order is the numeric order of the
+// logits); the row's top-k is among the union of those lists.  For k <= 32
+// each warp bitonic-sorts its lanes' maxima, and the largest warp's k-th
+// maximum -- a key that at least k keys reach -- bounds the slice's k-th
+// largest key from below; one more sweep collects the keys at or above it and
+// ranking them gives the exact top-k (heavy ties, or larger k, use the radix
+// selection of select_core.cuh).  Each CTA then stores its candidates
+// straight into rank 0's shared memory (st.shared::cluster) and, while rank 0
+// ranks the union (larger key first, equal keys by index), runs the FP64
+// top-p and stores the kept columns back into every CTA's shared memory,
+// writes -infinity over the rest of its slice: a logit outside its slice's
+// top-k cannot be kept.  After the second cluster barrier each CTA settles
+// its own candidates.  A split barrier at the start makes sure every CTA of
+// the cluster runs before the first remote store; nothing touches another
+// CTA's shared memory after the second barrier.  HBM traffic: the row read
+// once (its second sweep hits L2), written once.
 #include <atomic>
 
 #include "select_core.cuh"
@@ -31,28 +37,39 @@ namespace pgqa {
 namespace {
 
 constexpr int kMaskThreads = 512;
+constexpr int kMaskWarps = kMaskThreads / 32;
 constexpr int kMaskCtas = 8;            // CTAs per row: one cluster
-constexpr int kMaskSliceMax = 40960;    // logits a CTA stages (160 KB)
+constexpr int kMaskSliceMax = 40960;    // columns per CTA, at most
 constexpr int kMaskKMax = 128;          // largest k served
+constexpr int kWarpBoundK = 32;         // k up to which the warp-sorted bound is used
+constexpr int kFilterCap = 1024;        // keys the bound may let through
 using MaskShared = selcore::SelectShared<kMaskThreads, kMaskSliceMax / 32>;
 
-// Per-CTA state read across the cluster.
+// Shared state written across the cluster.
 struct MaskCluster {
+    int32_t cnt[kMaskCtas];                        // rank 0's copy: candidates of each CTA
+    uint32_t key[kMaskCtas * kMaskKMax];           //   ... their keys (slot r * kMaskKMax + i)
+    int32_t idx[kMaskCtas * kMaskKMax];            //   ... their columns
+    int32_t kept_n;                                // every copy: logits the row keeps
+    int32_t kept_idx[kMaskKMax];                   //   ... their columns
+};
+
+// Per-CTA scratch of the slice's top-k.
+struct MaskLocal {
+    uint32_t wkth[kMaskWarps];                     // each warp's k-th largest lane maximum
+    uint64_t comp[kFilterCap];                     // keys at or above the bound, as composites
+    int32_t n;
     int32_t cand_n;
-    int32_t kept_n;                         // rank 0: logits kept in the row
-    int32_t cand_idx[kMaskKMax];            // column of each candidate
-    uint32_t cand_key[kMaskKMax];
-    int32_t kept_idx[kMaskKMax];            // rank 0: their columns
+    uint32_t cand_key[kMaskKMax];                  // the slice's top-k
+    int32_t cand_idx[kMaskKMax];                   // (slice-relative columns)
 };
 
 // Rank 0's scratch for ranking the cluster's candidates.
 struct MaskMerge {
     int32_t base[kMaskCtas + 1];
-    int32_t cnt[kMaskCtas];
-    uint32_t key[kMaskCtas * kMaskKMax];
-    int32_t idx[kMaskCtas * kMaskKMax];
-    int32_t order[kMaskKMax];               // candidate at each rank
-    double s[kMaskKMax];                    // e_j, then the suffix sums S_j
+    uint64_t comp[kMaskCtas * kMaskKMax];          // the cluster's candidates, as composites
+    int32_t order[kMaskKMax];                      // candidate at each rank
+    double s[kMaskKMax];                           // e_j, then the suffix sums S_j
     int32_t m;
 };
 
@@ -63,12 +80,19 @@ __device__ __forceinline__ uint32_t cluster_rank()
     return r;
 }
 
-// Every thread of every CTA of the cluster; orders the shared-memory writes
-// before it against the reads after it, across the cluster.
-__device__ __forceinline__ void cluster_barrier()
+// Split cluster barrier: arrive (release or relaxed), later wait (acquire).
+// Every thread of every CTA of the cluster takes part.
+__device__ __forceinline__ void cluster_arrive_relaxed()
 {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
-                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait()
+{
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // Address of the same shared variable in CTA `rank` of the cluster.
@@ -79,11 +103,163 @@ __device__ __forceinline__ uint32_t dsmem(const void* p, uint32_t rank)
     return r;
 }
 
-__device__ __forceinline__ uint32_t ld_dsmem(uint32_t addr)
+__device__ __forceinline__ void st_dsmem(uint32_t addr, uint32_t v)
 {
-    uint32_t v;
-    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// A candidate as one 64-bit value whose unsigned order is the selection
+// order: the key above, the bitwise complement of the column below (a larger
+// key, or an equal key at a lower column, is larger).
+__device__ __forceinline__ uint64_t composite(uint32_t key, int col)
+{
+    return ((uint64_t)key << 32) | (uint32_t)~(uint32_t)col;
+}
+__device__ __forceinline__ uint32_t comp_key(uint64_t c) { return (uint32_t)(c >> 32); }
+__device__ __forceinline__ int comp_col(uint64_t c) { return (int)~(uint32_t)c; }
+
+// Rank of c among comp[0 .. n): how many are larger.
+__device__ __forceinline__ int rank_in(const uint64_t* comp, int n, uint64_t c)
+{
+    int better = 0;
+#pragma unroll 8
+    for (int u = 0; u < n; ++u)
+        better += comp[u] > c;
+    return better;
+}
+
+// The logit value of a key (ValueOrderKey maps -0 to +0; the value is the
+// same number).
+__device__ __forceinline__ float key_value(uint32_t k)
+{
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// Ascending bitonic sort of one value per lane across the warp.
+__device__ __forceinline__ uint32_t warp_sort_ascending(uint32_t v, int lane)
+{
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            const uint32_t o = __shfl_xor_sync(0xffffffffu, v, stride);
+            const bool asc = (lane & size) == 0, low = (lane & stride) == 0;
+            v = (asc == low) ? min(v, o) : max(v, o);
+        }
+    }
     return v;
+}
+
+// The top-k (k < n) of the slice's n keys, read from global memory, into
+// loc.cand_key / loc.cand_idx (any order; ties to the lower column).
+template <class Sh>
+__device__ void slice_top_k(const uint32_t* row, int n, int k, MaskLocal& loc, Sh& sh)
+{
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const selcore::ValueOrderKey key_of{};
+    if (k <= kWarpBoundK) {
+        // ---- each lane's largest key (0, below every logit's key, if none)
+        uint32_t mx = 0u;
+        if ((reinterpret_cast<uintptr_t>(row) & 15u) == 0) {
+            const int n4 = n >> 2;
+            const uint4* row4 = reinterpret_cast<const uint4*>(row);
+            constexpr int kUnroll = 8;
+            for (int j0 = tid; j0 < n4; j0 += kMaskThreads * kUnroll) {
+                uint4 v[kUnroll];
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) {
+                    const int j = j0 + u * kMaskThreads;
+                    v[u] = j < n4 ? __ldg(row4 + j) : make_uint4(0u, 0u, 0u, 0u);
+                }
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) {
+                    if (j0 + u * kMaskThreads < n4)
+                        mx = max(mx, max(max(key_of(v[u].x), key_of(v[u].y)),
+                                         max(key_of(v[u].z), key_of(v[u].w))));
+                }
+            }
+            for (int i = 4 * n4 + tid; i < n; i += kMaskThreads)
+                mx = max(mx, key_of(__ldg(row + i)));
+        } else {
+            for (int i = tid; i < n; i += kMaskThreads)
+                mx = max(mx, key_of(__ldg(row + i)));
+        }
+        // ---- bound: the largest warp's k-th largest lane maximum
+        const uint32_t sorted = warp_sort_ascending(mx, lane);
+        const uint32_t kth = __shfl_sync(0xffffffffu, sorted, 32 - k);
+        if (lane == 0)
+            loc.wkth[w] = kth;
+        if (tid == 0)
+            loc.n = 0;
+        __syncthreads();
+        uint32_t bound = 0u;
+        for (int v = 0; v < kMaskWarps; ++v)
+            bound = max(bound, loc.wkth[v]);
+        // ---- the keys at or above it (a second sweep; the slice is in L2 now)
+        auto collect = [&](bool hit, uint32_t kv, int i) {
+            const unsigned hits = __ballot_sync(0xffffffffu, hit);
+            if (hits != 0u) {
+                int base = 0;
+                if (lane == 0)
+                    base = atomicAdd(&loc.n, __popc(hits));
+                base = __shfl_sync(0xffffffffu, base, 0) + __popc(hits & ((1u << lane) - 1u));
+                if (hit && base < kFilterCap)
+                    loc.comp[base] = composite(kv, i);
+            }
+        };
+        int done = 0;
+        if ((reinterpret_cast<uintptr_t>(row) & 15u) == 0) {
+            const int n4 = n >> 2;
+            const uint4* row4 = reinterpret_cast<const uint4*>(row);
+            constexpr int kUnroll = 4;
+            for (int j0 = w * 32; j0 < n4; j0 += kMaskThreads * kUnroll) {
+                uint4 v[kUnroll];
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) {
+                    const int j = j0 + u * kMaskThreads + lane;
+                    v[u] = j < n4 ? __ldg(row4 + j) : make_uint4(0u, 0u, 0u, 0u);
+                }
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) {
+                    const int j = j0 + u * kMaskThreads + lane;
+                    const bool in = j < n4;
+                    const uint32_t k0 = key_of(v[u].x), k1 = key_of(v[u].y);
+                    const uint32_t k2 = key_of(v[u].z), k3 = key_of(v[u].w);
+                    collect(in && k0 >= bound, k0, 4 * j);
+                    collect(in && k1 >= bound, k1, 4 * j + 1);
+                    collect(in && k2 >= bound, k2, 4 * j + 2);
+                    collect(in && k3 >= bound, k3, 4 * j + 3);
+                }
+            }
+            done = 4 * n4;
+        }
+        for (int i0 = done + w * 32; i0 < n; i0 += kMaskThreads) {
+            const int i = i0 + lane;
+            const uint32_t kv = i < n ? key_of(__ldg(row + i)) : 0u;
+            collect(i < n && kv >= bound, kv, i);
+        }
+        __syncthreads();
+        const int C = loc.n;
+        if (C <= kFilterCap) {
+            for (int c = tid; c < C; c += kMaskThreads) {
+                const uint64_t cc = loc.comp[c];
+                const int better = rank_in(loc.comp, C, cc);
+                if (better < k) {
+                    loc.cand_key[better] = comp_key(cc);
+                    loc.cand_idx[better] = comp_col(cc);
+                }
+            }
+            __syncthreads();
+            return;
+        }
+    }
+    // ---- larger k, or a bound that lets too many keys through: radix selection
+    using Keys = selcore::GlobalKeys<selcore::ValueOrderKey>;
+    selcore::radix_select<false>(row, nullptr, Keys{row, key_of}, key_of, n, k, loc.cand_idx, sh);
+    __syncthreads();
+    for (int i = tid; i < k; i += kMaskThreads)
+        loc.cand_key[i] = key_of(__ldg(row + loc.cand_idx[i]));
+    __syncthreads();
 }
 
 }  // namespace
@@ -91,9 +267,11 @@ __device__ __forceinline__ uint32_t ld_dsmem(uint32_t addr)
 __global__ void __launch_bounds__(kMaskThreads, 1) topk_topp_kernel(MaskArgs a)
 {
     extern __shared__ __align__(16) unsigned char mask_smem[];
-    __shared__ MaskShared sh;
+    MaskShared& sh = *reinterpret_cast<MaskShared*>(mask_smem);   // radix state, candidate map
     __shared__ MaskCluster mc;
+    __shared__ MaskLocal loc;
     __shared__ MaskMerge mm;
+    cluster_arrive_relaxed();                     // paired with the wait before the first remote store
     const int tid = threadIdx.x;
     const uint32_t rank = cluster_rank();
     const int b = blockIdx.x / kMaskCtas;
@@ -103,67 +281,94 @@ __global__ void __launch_bounds__(kMaskThreads, 1) topk_topp_kernel(MaskArgs a)
     const int K = min(a.k, a.V);
     const selcore::ValueOrderKey key_of{};
 
-    // ---- this slice's top-k candidates (all of it when it has no more than k)
+    // ---- this slice's top-k (all of it when it has no more than k)
+    int cn;
     if (n > a.k) {
-        uint32_t* stage = reinterpret_cast<uint32_t*>(mask_smem);
-        selcore::radix_select<true>(row, stage, selcore::StagedKeys{stage}, key_of, n, a.k,
-                                    mc.cand_idx, sh);
-        __syncthreads();
-        for (int i = tid; i < a.k; i += kMaskThreads) {
-            const int li = mc.cand_idx[i];
-            mc.cand_key[i] = stage[li];
-            mc.cand_idx[i] = lo + li;
-        }
-        if (tid == 0)
-            mc.cand_n = a.k;
+        slice_top_k(row, n, a.k, loc, sh);
+        cn = a.k;
     } else {
         for (int i = tid; i < n; i += kMaskThreads) {
-            mc.cand_key[i] = key_of(__ldg(row + i));
-            mc.cand_idx[i] = lo + i;
+            loc.cand_key[i] = key_of(__ldg(row + i));
+            loc.cand_idx[i] = i;
         }
-        if (tid == 0)
-            mc.cand_n = n;
-    }
-    cluster_barrier();
-
-    // ---- rank 0: the row's top-k and top-p
-    if (rank == 0) {
-        if (tid < kMaskCtas)
-            mm.cnt[tid] = (int32_t)ld_dsmem(dsmem(&mc.cand_n, tid));
         __syncthreads();
+        cn = n;
+    }
+
+    // ---- candidates into rank 0's shared memory
+    cluster_wait();
+    if (tid == 0)
+        st_dsmem(dsmem(&mc.cnt[rank], 0), (uint32_t)cn);
+    for (int i = tid; i < cn; i += kMaskThreads) {
+        const int slot = (int)rank * kMaskKMax + i;
+        st_dsmem(dsmem(&mc.key[slot], 0), loc.cand_key[i]);
+        st_dsmem(dsmem(&mc.idx[slot], 0), (uint32_t)(lo + loc.cand_idx[i]));
+    }
+    cluster_arrive();
+
+    // ---- meanwhile: -inf over the slice except this CTA's candidates
+    uint32_t* cand_map = sh.above_map;                 // bit i: column lo + i is a candidate
+    const int nw = (n + 31) >> 5;
+    for (int w = tid; w < nw; w += kMaskThreads)
+        cand_map[w] = 0u;
+    __syncthreads();
+    for (int i = tid; i < cn; i += kMaskThreads)
+        atomicOr(&cand_map[loc.cand_idx[i] >> 5], 1u << (loc.cand_idx[i] & 31));
+    __syncthreads();
+    float* orow = a.out + (int64_t)b * a.out_stride + lo;
+    const float* xs = xrow + lo;
+    const float ninf = -INFINITY;
+    if ((reinterpret_cast<uintptr_t>(orow) & 15u) == 0) {
+        const int n4 = n >> 2;
+        for (int i4 = tid; i4 < n4; i4 += kMaskThreads) {
+            const uint32_t bits = (cand_map[i4 >> 3] >> ((i4 & 7) * 4)) & 15u;
+            if (bits == 0u) {
+                reinterpret_cast<float4*>(orow)[i4] = make_float4(ninf, ninf, ninf, ninf);
+            } else {
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    if (!((bits >> u) & 1u))
+                        orow[4 * i4 + u] = ninf;
+            }
+        }
+        for (int i = 4 * n4 + tid; i < n; i += kMaskThreads)
+            if (!((cand_map[i >> 5] >> (i & 31)) & 1u))
+                orow[i] = ninf;
+    } else {
+        for (int i = tid; i < n; i += kMaskThreads)
+            if (!((cand_map[i >> 5] >> (i & 31)) & 1u))
+                orow[i] = ninf;
+    }
+    cluster_wait();
+
+    // ---- rank 0: the row's top-k and top-p; kept columns into every CTA
+    if (rank == 0) {
         if (tid == 0) {
             mm.base[0] = 0;
             for (int r = 0; r < kMaskCtas; ++r)
-                mm.base[r + 1] = mm.base[r] + mm.cnt[r];
+                mm.base[r + 1] = mm.base[r] + mc.cnt[r];
         }
         __syncthreads();
         for (int r = 0; r < kMaskCtas; ++r) {
-            for (int i = tid; i < mm.cnt[r]; i += kMaskThreads) {
-                mm.key[mm.base[r] + i] = ld_dsmem(dsmem(&mc.cand_key[i], r));
-                mm.idx[mm.base[r] + i] = (int32_t)ld_dsmem(dsmem(&mc.cand_idx[i], r));
-            }
+            for (int i = tid; i < mc.cnt[r]; i += kMaskThreads)
+                mm.comp[mm.base[r] + i] = composite(mc.key[r * kMaskKMax + i],
+                                                    mc.idx[r * kMaskKMax + i]);
         }
         __syncthreads();
         const int T = mm.base[kMaskCtas];
         for (int c = tid; c < T; c += kMaskThreads) {
-            const uint32_t kc = mm.key[c];
-            const int ic = mm.idx[c];
-            int better = 0;
-            for (int u = 0; u < T; ++u) {
-                const uint32_t ku = mm.key[u];
-                better += ku > kc || (ku == kc && mm.idx[u] < ic);
-            }
+            const int better = rank_in(mm.comp, T, mm.comp[c]);
             if (better < K)
                 mm.order[better] = c;
         }
         __syncthreads();
-        // FP64 masses of the top-K logits, read back from the row itself
-        const float x0f = __ldg(xrow + mm.idx[mm.order[0]]);
+        // FP64 masses of the top-K logits (their values are their keys mapped back)
+        const float x0f = key_value(comp_key(mm.comp[mm.order[0]]));
         const bool usable = !(isnan(x0f) || isinf(x0f));   // -inf, +inf or NaN at the top
         if (usable) {
             const double x0 = (double)x0f;
             for (int j = tid; j < K; j += kMaskThreads)
-                mm.s[j] = exp((double)__ldg(xrow + mm.idx[mm.order[j]]) - x0);
+                mm.s[j] = exp((double)key_value(comp_key(mm.comp[mm.order[j]])) - x0);
         }
         __syncthreads();
         if (tid == 0) {
@@ -182,65 +387,33 @@ __global__ void __launch_bounds__(kMaskThreads, 1) topk_topp_kernel(MaskArgs a)
                 raise_flag(a.err, PAGED_GQA_FLAG_BAD_LOGIT);
             }
             mm.m = m;
-            mc.kept_n = m;
         }
         __syncthreads();
-        for (int j = tid; j < mm.m; j += kMaskThreads)
-            mc.kept_idx[j] = mm.idx[mm.order[j]];
+        const int m = mm.m;
+        for (int t = tid; t < kMaskCtas * (m + 1); t += kMaskThreads) {
+            const int r = t / (m + 1), j = t - r * (m + 1);
+            if (j == m)
+                st_dsmem(dsmem(&mc.kept_n, r), (uint32_t)m);
+            else
+                st_dsmem(dsmem(&mc.kept_idx[j], r), (uint32_t)comp_col(mm.comp[mm.order[j]]));
+        }
     }
-    cluster_barrier();
+    cluster_arrive();
+    cluster_wait();
 
-    // ---- this slice: -inf except the kept logits
-    const int m = (int)ld_dsmem(dsmem(&mc.kept_n, 0));
-    uint32_t* kept = sh.above_map;                      // free again: bit i = column lo + i kept
-    const int nw = (n + 31) >> 5;
-    for (int w = tid; w < nw; w += kMaskThreads)
-        kept[w] = 0u;
-    __syncthreads();
-    for (int j = tid; j < m; j += kMaskThreads) {
-        const int col = (int)ld_dsmem(dsmem(&mc.kept_idx[j], 0));
-        if (col >= lo && col < hi)
-            atomicOr(&kept[(col - lo) >> 5], 1u << ((col - lo) & 31));
-    }
-    __syncthreads();
-    float* orow = a.out + (int64_t)b * a.out_stride + lo;
-    const float* xs = xrow + lo;
+    // ---- this CTA's candidates: kept ones carry their logit, the others -inf
+    const int m = mc.kept_n;
     const bool in_place = orow == xs;
-    const float ninf = -INFINITY;
-    if ((reinterpret_cast<uintptr_t>(orow) & 15u) == 0) {
-        const int n4 = n >> 2;
-        for (int i4 = tid; i4 < n4; i4 += kMaskThreads) {
-            const uint32_t bits = (kept[i4 >> 3] >> ((i4 & 7) * 4)) & 15u;
-            if (bits == 0u) {
-                reinterpret_cast<float4*>(orow)[i4] = make_float4(ninf, ninf, ninf, ninf);
-            } else {
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int i = 4 * i4 + u;
-                    if (!((bits >> u) & 1u))
-                        orow[i] = ninf;
-                    else if (!in_place)
-                        orow[i] = xs[i];
-                }
-            }
-        }
-        for (int i = 4 * n4 + tid; i < n; i += kMaskThreads) {
-            const bool k1 = (kept[i >> 5] >> (i & 31)) & 1u;
-            if (!k1)
-                orow[i] = ninf;
-            else if (!in_place)
-                orow[i] = xs[i];
-        }
-    } else {
-        for (int i = tid; i < n; i += kMaskThreads) {
-            const bool k1 = (kept[i >> 5] >> (i & 31)) & 1u;
-            if (!k1)
-                orow[i] = ninf;
-            else if (!in_place)
-                orow[i] = xs[i];
-        }
+    for (int i = tid; i < cn; i += kMaskThreads) {
+        const int col = lo + loc.cand_idx[i];
+        bool keep = false;
+        for (int j = 0; j < m; ++j)
+            keep |= mc.kept_idx[j] == col;
+        if (!keep)
+            orow[loc.cand_idx[i]] = ninf;
+        else if (!in_place)
+            orow[loc.cand_idx[i]] = xs[loc.cand_idx[i]];
     }
-    cluster_barrier();                                  // rank 0's lists were read by all
 }
 
 int mask_slice(int V)
@@ -263,7 +436,7 @@ cudaError_t launch_topk_topp(const MaskArgs& a, cudaStream_t s)
         return e;
     if (dev >= kMaxDevices || !done[dev].load(std::memory_order_acquire)) {
         e = cudaFuncSetAttribute(topk_topp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)(kMaskSliceMax * sizeof(uint32_t)));
+                                 (int)sizeof(MaskShared));
         if (e != cudaSuccess)
             return e;
         if (dev < kMaxDevices)
@@ -272,7 +445,7 @@ cudaError_t launch_topk_topp(const MaskArgs& a, cudaStream_t s)
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)a.B * kMaskCtas);
     cfg.blockDim = dim3(kMaskThreads);
-    cfg.dynamicSmemBytes = (size_t)a.slice * sizeof(uint32_t);
+    cfg.dynamicSmemBytes = sizeof(MaskShared);
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
