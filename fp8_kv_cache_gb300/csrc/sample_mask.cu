@@ -13,12 +13,12 @@
 // Design (ours): one thread-block cluster of kMaskCtas CTAs per row, so a
 // handful of rows still spreads over the GPU.  Each CTA finds the top-k of
 // its slice of the row (keys whose unsigned order is the numeric order of the
-// logits); the row's top-k is among the union of those lists.  For k <= 32
-// each warp bitonic-sorts its lanes' maxima, and the largest warp's k-th
-// maximum -- a key that at least k keys reach -- bounds the slice's k-th
-// largest key from below; one more sweep collects the keys at or above it and
-// ranking them gives the exact top-k (heavy ties, or larger k, use the radix
-// selection of select_core.cuh).  Each CTA then stores its candidates
+// logits); the row's top-k is among the union of those lists.  The CTA
+// bitonic-sorts its threads' maxima, and their k-th largest -- a key that at
+// least k keys reach -- bounds the slice's k-th largest key from below; one
+// more sweep collects the keys at or above it (typically a few more than k)
+// and ranking them gives the exact top-k (a tie-saturated slice, where too
+// many keys reach the bound, uses the radix selection of select_core.cuh).  Each CTA then stores its candidates
 // straight into rank 0's shared memory (st.shared::cluster) and, while rank 0
 // ranks the union (larger key first, equal keys by index), runs the FP64
 // top-p and stores the kept columns back into every CTA's shared memory,
@@ -41,7 +41,7 @@ constexpr int kMaskWarps = kMaskThreads / 32;
 constexpr int kMaskCtas = 8;            // CTAs per row: one cluster
 constexpr int kMaskSliceMax = 40960;    // columns per CTA, at most
 constexpr int kMaskKMax = 128;          // largest k served
-constexpr int kWarpBoundK = 32;         // k up to which the warp-sorted bound is used
+constexpr int kBoundK = kMaskThreads;   // k up to which the threads' maxima give the bound
 constexpr int kFilterCap = 1024;        // keys the bound may let through
 using MaskShared = selcore::SelectShared<kMaskThreads, kMaskSliceMax / 32>;
 
@@ -56,7 +56,8 @@ struct MaskCluster {
 
 // Per-CTA scratch of the slice's top-k.
 struct MaskLocal {
-    uint32_t wkth[kMaskWarps];                     // each warp's k-th largest lane maximum
+    uint32_t sortbuf[kMaskThreads];                // the lanes' maxima while they are sorted
+    uint32_t bound;
     uint64_t comp[kFilterCap];                     // keys at or above the bound, as composites
     int32_t n;
     int32_t cand_n;
@@ -135,15 +136,26 @@ __device__ __forceinline__ float key_value(uint32_t k)
     return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-// Ascending bitonic sort of one value per lane across the warp.
-__device__ __forceinline__ uint32_t warp_sort_ascending(uint32_t v, int lane)
+// Ascending bitonic sort of one value per thread across the CTA: partners
+// closer than a warp trade through shuffles, the others through buf (one
+// slot per thread).  Thread t ends with the t-th smallest value.
+__device__ __forceinline__ uint32_t block_sort_ascending(uint32_t v, uint32_t* buf)
 {
+    const int tid = threadIdx.x;
 #pragma unroll
-    for (int size = 2; size <= 32; size <<= 1) {
+    for (int size = 2; size <= kMaskThreads; size <<= 1) {
 #pragma unroll
         for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            const uint32_t o = __shfl_xor_sync(0xffffffffu, v, stride);
-            const bool asc = (lane & size) == 0, low = (lane & stride) == 0;
+            uint32_t o;
+            if (stride >= 32) {
+                buf[tid] = v;
+                __syncthreads();
+                o = buf[tid ^ stride];
+                __syncthreads();
+            } else {
+                o = __shfl_xor_sync(0xffffffffu, v, stride);
+            }
+            const bool asc = (tid & size) == 0, low = (tid & stride) == 0;
             v = (asc == low) ? min(v, o) : max(v, o);
         }
     }
@@ -157,8 +169,8 @@ __device__ void slice_top_k(const uint32_t* row, int n, int k, MaskLocal& loc, S
 {
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const selcore::ValueOrderKey key_of{};
-    if (k <= kWarpBoundK) {
-        // ---- each lane's largest key (0, below every logit's key, if none)
+    if (k <= kBoundK) {
+        // ---- each thread's largest key (0, below every logit's key, if none)
         uint32_t mx = 0u;
         if ((reinterpret_cast<uintptr_t>(row) & 15u) == 0) {
             const int n4 = n >> 2;
@@ -184,17 +196,14 @@ __device__ void slice_top_k(const uint32_t* row, int n, int k, MaskLocal& loc, S
             for (int i = tid; i < n; i += kMaskThreads)
                 mx = max(mx, key_of(__ldg(row + i)));
         }
-        // ---- bound: the largest warp's k-th largest lane maximum
-        const uint32_t sorted = warp_sort_ascending(mx, lane);
-        const uint32_t kth = __shfl_sync(0xffffffffu, sorted, 32 - k);
-        if (lane == 0)
-            loc.wkth[w] = kth;
+        // ---- bound: the k-th largest of the threads' maxima
+        const uint32_t sorted = block_sort_ascending(mx, loc.sortbuf);
+        if (tid == kMaskThreads - k)
+            loc.bound = sorted;
         if (tid == 0)
             loc.n = 0;
         __syncthreads();
-        uint32_t bound = 0u;
-        for (int v = 0; v < kMaskWarps; ++v)
-            bound = max(bound, loc.wkth[v]);
+        const uint32_t bound = loc.bound;
         // ---- the keys at or above it (a second sweep; the slice is in L2 now)
         auto collect = [&](bool hit, uint32_t kv, int i) {
             const unsigned hits = __ballot_sync(0xffffffffu, hit);
@@ -207,36 +216,38 @@ __device__ void slice_top_k(const uint32_t* row, int n, int k, MaskLocal& loc, S
                     loc.comp[base] = composite(kv, i);
             }
         };
-        int done = 0;
-        if ((reinterpret_cast<uintptr_t>(row) & 15u) == 0) {
-            const int n4 = n >> 2;
-            const uint4* row4 = reinterpret_cast<const uint4*>(row);
-            constexpr int kUnroll = 4;
-            for (int j0 = w * 32; j0 < n4; j0 += kMaskThreads * kUnroll) {
-                uint4 v[kUnroll];
+        {
+            int done = 0;
+            if ((reinterpret_cast<uintptr_t>(row) & 15u) == 0) {
+                const int n4 = n >> 2;
+                const uint4* row4 = reinterpret_cast<const uint4*>(row);
+                constexpr int kUnroll = 4;
+                for (int j0 = w * 32; j0 < n4; j0 += kMaskThreads * kUnroll) {
+                    uint4 v[kUnroll];
 #pragma unroll
-                for (int u = 0; u < kUnroll; ++u) {
-                    const int j = j0 + u * kMaskThreads + lane;
-                    v[u] = j < n4 ? __ldg(row4 + j) : make_uint4(0u, 0u, 0u, 0u);
-                }
+                    for (int u = 0; u < kUnroll; ++u) {
+                        const int j = j0 + u * kMaskThreads + lane;
+                        v[u] = j < n4 ? __ldg(row4 + j) : make_uint4(0u, 0u, 0u, 0u);
+                    }
 #pragma unroll
-                for (int u = 0; u < kUnroll; ++u) {
-                    const int j = j0 + u * kMaskThreads + lane;
-                    const bool in = j < n4;
-                    const uint32_t k0 = key_of(v[u].x), k1 = key_of(v[u].y);
-                    const uint32_t k2 = key_of(v[u].z), k3 = key_of(v[u].w);
-                    collect(in && k0 >= bound, k0, 4 * j);
-                    collect(in && k1 >= bound, k1, 4 * j + 1);
-                    collect(in && k2 >= bound, k2, 4 * j + 2);
-                    collect(in && k3 >= bound, k3, 4 * j + 3);
+                    for (int u = 0; u < kUnroll; ++u) {
+                        const int j = j0 + u * kMaskThreads + lane;
+                        const bool in = j < n4;
+                        const uint32_t k0 = key_of(v[u].x), k1 = key_of(v[u].y);
+                        const uint32_t k2 = key_of(v[u].z), k3 = key_of(v[u].w);
+                        collect(in && k0 >= bound, k0, 4 * j);
+                        collect(in && k1 >= bound, k1, 4 * j + 1);
+                        collect(in && k2 >= bound, k2, 4 * j + 2);
+                        collect(in && k3 >= bound, k3, 4 * j + 3);
+                    }
                 }
+                done = 4 * n4;
             }
-            done = 4 * n4;
-        }
-        for (int i0 = done + w * 32; i0 < n; i0 += kMaskThreads) {
-            const int i = i0 + lane;
-            const uint32_t kv = i < n ? key_of(__ldg(row + i)) : 0u;
-            collect(i < n && kv >= bound, kv, i);
+            for (int i0 = done + w * 32; i0 < n; i0 += kMaskThreads) {
+                const int i = i0 + lane;
+                const uint32_t kv = i < n ? key_of(__ldg(row + i)) : 0u;
+                collect(i < n && kv >= bound, kv, i);
+            }
         }
         __syncthreads();
         const int C = loc.n;
