@@ -18,7 +18,8 @@ The same line reports the selected-sparse prefill (4096 rows, 512 selected
 four-token blocks + a 1..3-token tail, Hq6/Hkv1/D256 FP16, interleaved K/V,
 32768-token cache) timed the same way, the same prefill over an E4M3 copy of
 the cache, the QSA block selection that produces such selections (4096 rows
-of 8192 block scores, k = 512), the roofline of the dominant kernel
+of 8192 block scores, k = 512), the decode step's top-k/top-p masking of
+16 x 248,320 logits (k = 20, p = 0.95), the roofline of the dominant kernel
 (the decode split kernel, timed by CUDA events the library records around it
 on the launching stream), an end-to-end number through host buffers, SM
 clocks sampled during the timed phases, and the FP64 CPU oracle timed on a
@@ -192,6 +193,8 @@ def run_ours(args, rank, world):
         return run_prefill_only(args, dev)
     if args.phase == "select":
         return run_select_only(args, dev)
+    if args.phase == "mask":
+        return run_mask_only(args, dev)
     case = W.long_e4m3()
     kvb = decode_kv_bytes(case)
     kv = torch.from_numpy(case.kv).to(dev)
@@ -380,6 +383,12 @@ def run_ours(args, rank, world):
     s_out = torch.empty((sc.scores.shape[0], sc.k), dtype=torch.int32, device=dev)
     s_ms = time_phase(lambda: P.paged_gqa_select_blocks(s_scores, s_qpos, sc.kv_len, sc.k,
                                                         out=s_out))
+    # ---- top-k/top-p masking of the decode step's logits: B16 x 248,320
+    mc_ = W.sampler_b16()
+    m_x = torch.from_numpy(mc_.logits).to(dev)
+    m_out = torch.empty_like(m_x)
+    m_ms = time_phase(lambda: P.paged_gqa_topk_topp_mask(m_x, mc_.k, mc_.p, out=m_out))
+    m_bytes = 2 * mc_.logits.nbytes                            # the logits read once, written once
     clocks.stop()
     s_rows = sc.scores.shape[0]
     s_cands = int(np.minimum(sc.q_pos.astype(np.int64) // 4, sc.n_blocks).sum())
@@ -451,6 +460,14 @@ def run_ours(args, rank, world):
             "GBps": round(s_bytes / (s_ms * 1e-3) / 1e9, 1),
             "hbm_frac": round(s_bytes / (s_ms * 1e-3) / 1e9 / peak, 4),
         },
+        "topk_topp_mask": {
+            "workload": "16 rows of 248,320 float32 logits, top-k 20 then top-p 0.95, "
+                        "N(0, 2.5^2) with 32 raised positions per row",
+            "ms": round(m_ms, 4), "rows_per_s": round(world * mc_.logits.shape[0] / (m_ms * 1e-3), 1),
+            "algorithmic_bytes": m_bytes,
+            "GBps": round(m_bytes / (m_ms * 1e-3) / 1e9, 1),
+            "hbm_frac": round(m_bytes / (m_ms * 1e-3) / 1e9 / peak, 4),
+        },
         "gpu_launches": 2 * K,
         "clocks": clocks.summary(),
         "wall_s_timed_decode": round(wall, 4),
@@ -503,6 +520,26 @@ def run_select_only(args, dev):
         if i >= args.warmup:
             ms.append(a.elapsed_time(b))
     return {"phase": "select", "ms": float(np.mean(ms))}
+
+
+def run_mask_only(args, dev):
+    """The top-k/top-p masking phase alone (for profiling)."""
+    import torch
+    import fp8_kv_cache_gb300 as P
+    from fp8_kv_cache_gb300 import workloads as W
+    mc_ = W.sampler_b16()
+    m_x = torch.from_numpy(mc_.logits).to(dev)
+    m_out = torch.empty_like(m_x)
+    ms = []
+    for i in range(args.warmup + args.steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        P.paged_gqa_topk_topp_mask(m_x, mc_.k, mc_.p, out=m_out)
+        b.record()
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            ms.append(a.elapsed_time(b))
+    return {"phase": "mask", "ms": float(np.mean(ms))}
 
 
 def cpu_baseline(sample_seqs=4, threads=None):
@@ -573,7 +610,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--phase", choices=["all", "decode", "prefill", "select"], default="all",
+    ap.add_argument("--phase", choices=["all", "decode", "prefill", "select", "mask"],
+                    default="all",
                     help="run only one phase (for profiling); the JSON line needs 'all'")
     args = ap.parse_args()
     if args.warmup < 3:
