@@ -213,13 +213,17 @@ def e4m3_b8(seed=2):
                        seed=seed)
 
 
-def long_e4m3(seed=3, B=16):
+def long_e4m3(seed=3, B=16, page_size=16):
     """B=16, Hkv=4, Hq=24, seq_lens uniform in [12288, 16384], shuffled pool of
-    16384 pages of 16, E4M3 KV from N(0,1)*2."""
+    16384 pages of 16 (or the same tokens in pages of page_size), E4M3 KV from
+    N(0,1)*2."""
     rng = np.random.default_rng(seed + 1000)
     lens = rng.integers(12288, 16384, size=B, endpoint=True).astype(np.int32)
-    return decode_case(f"long_e4m3_b{B}", B=B, Hq=24, Hkv=4, seq_lens=lens, kv_dtype="e4m3",
-                       seed=seed, max_seq_len=16384, num_pages=B * 1024)
+    pages = B * (-(-16384 // page_size))
+    suffix = "" if page_size == 16 else f"_p{page_size}"
+    return decode_case(f"long_e4m3_b{B}{suffix}", B=B, Hq=24, Hkv=4, seq_lens=lens,
+                       kv_dtype="e4m3", seed=seed, max_seq_len=16384, num_pages=pages,
+                       page_size=page_size)
 
 
 def sweep(B, L, kv_dtype, seed=4):

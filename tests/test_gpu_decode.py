@@ -77,7 +77,7 @@ def test_sweep(B, L, kvd):
 # ---------------------------------------------------------------- shapes and edges
 
 @pytest.mark.parametrize("kvd", ["fp16", "e4m3"])
-@pytest.mark.parametrize("page_size", [16, 4, 48, 784])
+@pytest.mark.parametrize("page_size", [16, 4, 48, 64, 128, 256, 784])
 def test_ragged_lengths_and_page_sizes(page_size, kvd):
     lens = [1, 7, 8, 9, 15, 16, 17, 31, 33, 100, 257, 1500]
     c = W.decode_case(f"ragged_p{page_size}_{kvd}", B=len(lens), Hq=12, Hkv=2, seq_lens=lens,
