@@ -84,6 +84,22 @@ def test_special_values():
         _check(sc, qp, 4 * nb + 4, k, what=f"specials k={k}")
 
 
+@pytest.mark.parametrize("k", [100, 700, 1400])
+def test_bucket_sizes(k):
+    """Rows whose pivot falls in a first-digit bucket of 1500 keys (values in
+    [1, 1.25) share their first 11 key bits): larger than the buckets ranked
+    outright, so the later digits are histogrammed."""
+    rng = np.random.default_rng(310 + k)
+    R, nb = 8, 8000
+    sc = -rng.random((R, nb)).astype(np.float32)                 # below the bucket
+    idx = rng.random((R, nb)).argsort(axis=1)[:, :1500]
+    vals = (1.0 + 0.25 * rng.random((R, 1500))).astype(np.float32)
+    np.put_along_axis(sc, idx, vals, axis=1)
+    sc[1] = np.round(sc[1] * 64) / 64                           # ties inside the bucket
+    qp = np.full(R, 4 * nb + 1, dtype=np.int32)
+    _check(sc, qp, 4 * nb + 4, k, what=f"bucket k={k}")
+
+
 def test_inert_rows_and_flags():
     rng = np.random.default_rng(302)
     sc = rng.standard_normal((8, 100)).astype(np.float32)
