@@ -102,7 +102,7 @@ int check_decode_shape(int B, int Hq, int Hkv, int D, int max_seq_len)
 {
     if (B < 0 || Hq < 1 || Hkv < 1 || max_seq_len < 0)
         return PAGED_GQA_ERR_SHAPE;
-    if (Hq % Hkv != 0)
+    if (Hq % Hkv != 0 || (int64_t)B * Hq > INT32_MAX)   // one CTA per (b, KV head) at most
         return PAGED_GQA_ERR_SHAPE;
     if (D != kD || Hq / Hkv > kGMax)
         return PAGED_GQA_ERR_UNSUPPORTED;
@@ -338,7 +338,8 @@ int paged_gqa_topk_topp_mask(const float* logits, int64_t logits_stride, float* 
                              int64_t out_stride, int B, int V, int k, float p, int* err_flag,
                              void* stream)
 {
-    if (B < 0 || V < 1 || logits_stride < V || out_stride < V || !(p > 0.f && p <= 1.f))
+    if (B < 0 || B > (1 << 27) || V < 1 || logits_stride < V || out_stride < V ||
+        !(p > 0.f && p <= 1.f))
         return PAGED_GQA_ERR_SHAPE;
     if (!mask_supported(V, k))
         return k < 1 ? PAGED_GQA_ERR_SHAPE : PAGED_GQA_ERR_UNSUPPORTED;

@@ -259,6 +259,7 @@ int paged_gqa_select_blocks(const float* scores, int64_t score_stride, int n_blo
  *  k             1 .. 128.
  *  p             0 < p <= 1 (p = 1: top-k alone).
  *  V             1 .. 327680.
+ *  B             0 .. 2^27 rows (8 CTAs each).
  *  err_flag      optional device int receiving PAGED_GQA_FLAG_* bits.
  * One kernel is launched: a cluster of 8 CTAs per row; nothing is allocated.
  */

@@ -104,6 +104,7 @@ def _decode(L, **kw):
     (dict(B=-1), -3), (dict(Hq=0), -3), (dict(Hkv=0), -3), (dict(Hq=25), -3),
     (dict(P=0), -3), (dict(num_pages=0), -3), (dict(max_seq_len=-1), -3),
     (dict(bt_stride=100), -3), (dict(layout=(-1, 256, 256)), -3),
+    (dict(B=(1 << 27), Hq=24, Hkv=4), -3),                   # B * Hq beyond one launch
     (dict(D=128), -4), (dict(Hq=36, Hkv=4), -4), (dict(dtype=2), -4),
 ])
 @host_only
@@ -197,6 +198,8 @@ def test_topk_topp_mask_validates(L):
     for p in (0.0, -0.5, 1.5, float("nan")):
         assert L.paged_gqa_topk_topp_mask(A, 1000, A + 4096, 1000, 4, 1000, 20, p, None, None) == -3
     assert L.paged_gqa_topk_topp_mask(A, 1000, A, 1024, 4, 1000, 20, 0.95, None, None) == -3
+    assert L.paged_gqa_topk_topp_mask(A, 1000, A + 4096, 1000, (1 << 27) + 1, 1000, 20, 0.95,
+                                      None, None) == -3
     assert L.paged_gqa_topk_topp_mask(A, 1000, A + 4096, 1000, 0, 1000, 20, 0.95, None, None) == 0
 
 

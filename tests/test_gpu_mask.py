@@ -87,6 +87,12 @@ def test_vocab_sizes(V):
     _check(c.logits, min(20, 128), 0.9, f"V={V}")
 
 
+def test_many_rows():
+    """300 rows: many waves of clusters."""
+    c = W.logits_case("many", B=300, V=3000, seed=506, peaks=8)
+    _check(c.logits, 20, 0.95, "B=300")
+
+
 def test_strided_and_in_place():
     c = W.logits_case("strided", B=4, V=30001, seed=503)
     want, _ = oracle.topk_topp_mask(c.logits, 20, 0.95)
