@@ -339,21 +339,21 @@ def run_ours(args, rank, world):
     Kp = max(1, min(K, 50))
 
     def time_phase(fn):
-        """Mean ms of Kp launches of fn, each between L2 flushes."""
+        """Mean ms of Kp launches of fn, each between L2 flushes.  Everything
+        is queued before one synchronisation, as in the headline loop, so the
+        host's launch overhead does not fall inside the events."""
         for _ in range(max(3, Wm)):
             fn()
             flush_l2()
         torch.cuda.synchronize()
-        total = 0.0
-        for _ in range(Kp):
-            a, b = mk(), mk()
-            a.record()
+        a_ev, b_ev = [mk() for _ in range(Kp)], [mk() for _ in range(Kp)]
+        for i in range(Kp):
+            a_ev[i].record()
             fn()
-            b.record()
+            b_ev[i].record()
             flush_l2()
-            torch.cuda.synchronize()
-            total += a.elapsed_time(b)
-        return total / Kp
+        torch.cuda.synchronize()
+        return sum(a_ev[i].elapsed_time(b_ev[i]) for i in range(Kp)) / Kp
 
     # ---- selected-sparse prefill, 4096 rows, FP16 and E4M3 caches
     def prefill_phase(kv_dtype):
