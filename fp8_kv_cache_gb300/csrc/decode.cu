@@ -226,17 +226,21 @@ __global__ void __launch_bounds__(kThreads, kMinCtas<kE4M3>()) decode_split_kern
 // griddepcontrol.wait; after it, one round of loads brings every piece's
 // (m, l, O) in.  Batches above kMergeScanMax read the prefix the split kernel
 // leaves in the workspace header instead, after the wait.
-__global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeArgs a)
+__global__ void __launch_bounds__(kMergeThreads * kMergeGroups) decode_merge_kernel(DecodeArgs a)
 {
-    __shared__ int64_t red_s[2][2];
+    constexpr int kThreadsAll = kMergeThreads * kMergeGroups;
+    __shared__ int64_t red_s[kThreadsAll / 32][2];
+    __shared__ float g_m[kMergeGroups], g_den[kMergeGroups];
+    __shared__ float4 g_num[kMergeGroups][kMergeThreads];
     const int h = blockIdx.x, b = blockIdx.y;
     const int j = h / a.G, hh = h - j * a.G;
-    const int tid = threadIdx.x, d = 4 * tid;
+    const int tid = threadIdx.x, grp = tid / kMergeThreads, gt = tid % kMergeThreads;
+    const int d = 4 * gt;
     __half2* out2 = reinterpret_cast<__half2*>(a.out + ((size_t)b * a.Hq + h) * kD + d);
     int64_t before, total;     // line tiles of sequences < b, of all sequences
     if (a.B <= kMergeScanMax) {
         int64_t lo = 0, all = 0;
-        for (int i = tid; i < a.B; i += kMergeThreads) {
+        for (int i = tid; i < a.B; i += kThreadsAll) {
             const int64_t n = seg_len(a, i);
             all += n;
             lo += i < b ? n : 0;
@@ -251,8 +255,12 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeArgs 
             red_s[tid >> 5][1] = all;
         }
         __syncthreads();
-        before = red_s[0][0] + red_s[1][0];
-        total = red_s[0][1] + red_s[1][1];
+        before = 0;
+        total = 0;
+        for (int w = 0; w < kThreadsAll / 32; ++w) {
+            before += red_s[w][0];
+            total += red_s[w][1];
+        }
     } else {
         asm volatile("griddepcontrol.wait;" ::: "memory");
         before = a.hdr[2 + b];
@@ -262,8 +270,10 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeArgs 
     // this grid always implies the end of the split grid.
     const int64_t nb = seg_len(a, b);
     if (nb == 0) {                               // the split kernel never writes these rows
-        out2[0] = __floats2half2_rn(0.f, 0.f);
-        out2[1] = __floats2half2_rn(0.f, 0.f);
+        if (grp == 0) {
+            out2[0] = __floats2half2_rn(0.f, 0.f);
+            out2[1] = __floats2half2_rn(0.f, 0.f);
+        }
         asm volatile("griddepcontrol.wait;" ::: "memory");
         return;
     }
@@ -282,7 +292,13 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeArgs 
     float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
     float den = 0.f, M_run = -INFINITY;
     constexpr int kChunk = 8;
-    for (int64_t c0 = c_first; c0 <= c_last; c0 += kChunk) {
+    // Chunks of kChunk pieces go to the kMergeGroups thread groups in turn;
+    // a segment of one chunk is merged by group 0 alone.
+    const bool grouped = c_last - c_first + 1 > kChunk;      // CTA-uniform
+    if (!grouped && grp != 0)
+        return;
+    for (int64_t c0 = c_first + (int64_t)grp * kChunk; c0 <= c_last;
+         c0 += (int64_t)(grouped ? kMergeGroups : 1) * kChunk) {
         const int np = (int)min((int64_t)kChunk, c_last - c0 + 1);
         const float* sl0 = base + (size_t)(c0 - c_first) * kSlotFloats;
         float m[kChunk], l[kChunk];
@@ -320,6 +336,33 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeArgs 
             num.y += e * o[i].y;
             num.z += e * o[i].z;
             num.w += e * o[i].w;
+        }
+    }
+    if (grouped) {
+        // the groups' states, combined in group order
+        if (gt == 0) {
+            g_m[grp] = M_run;
+            g_den[grp] = den;
+        }
+        g_num[grp][gt] = num;
+        __syncthreads();
+        if (grp != 0)
+            return;
+        float M = -INFINITY;
+        for (int g = 0; g < kMergeGroups; ++g)
+            M = fmaxf(M, g_m[g]);
+        num = make_float4(0.f, 0.f, 0.f, 0.f);
+        den = 0.f;
+        if (M != -INFINITY) {
+            for (int g = 0; g < kMergeGroups; ++g) {
+                const float e = g_m[g] == -INFINITY ? 0.f : ex2(g_m[g] - M);
+                const float4 o = g_num[g][gt];
+                den += e * g_den[g];
+                num.x += e * o.x;
+                num.y += e * o.y;
+                num.z += e * o.z;
+                num.w += e * o.w;
+            }
         }
     }
     const float sc = den > 0.f ? a.v_scale / den : 0.f;
@@ -394,7 +437,7 @@ cudaError_t launch_decode(const DecodeArgs& a, bool e4m3, cudaStream_t s, void* 
     if (a.C > 0) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(a.Hq, a.B);
-        cfg.blockDim = dim3(kMergeThreads);
+        cfg.blockDim = dim3(kMergeThreads * kMergeGroups);
         cfg.dynamicSmemBytes = 0;
         cfg.stream = s;
         cudaLaunchAttribute attr[1];

@@ -10,7 +10,8 @@
 namespace pgqa {
 
 constexpr int kMaxSplitBatch = 4096;   // split route keeps a (B+1) prefix in shared memory
-constexpr int kMergeThreads = 64;     // 4 head-dim values per thread
+constexpr int kMergeThreads = 64;     // threads of a merge group: 4 head-dim values each
+constexpr int kMergeGroups = 4;       // groups of a merge CTA, taking chunks of pieces in turn
 constexpr int kMergeScanMax = 512;    // merge recomputes the cut from seq_lens up to this batch
 constexpr int kHeaderBytes = 64;       // workspace header: T, C_eff
 constexpr int kMaxDevices = 64;        // per-device caches
