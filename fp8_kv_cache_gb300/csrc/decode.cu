@@ -52,13 +52,18 @@ __device__ __forceinline__ int64_t seg_len(const DecodeArgs& a, int b)
 }
 
 // CTAs that take part in the cut of a line of T > 0 tiles: at most the
-// launched C, at most ceil(T / min_tiles) when min_tiles > 0, and at most T,
-// so every one of them gets a non-empty range.
+// launched C and at most T, so every one of them gets a non-empty range; when
+// min_tiles > 0, each gets at least min_tiles tiles, or twice that while the
+// line still fills half the launched CTAs (longer ranges mean fewer pieces to
+// merge and longer pipelines, which pays for long single sequences; short
+// lines keep the parallelism).
 __device__ __forceinline__ int64_t effective_ctas(const DecodeArgs& a, int64_t T)
 {
     int64_t C = a.C;
-    if (a.min_tiles > 0)
-        C = min(C, (T + a.min_tiles - 1) / a.min_tiles);
+    if (a.min_tiles > 0) {
+        const int64_t c_long = T / (2 * a.min_tiles);
+        C = min(C, c_long >= C / 2 ? c_long : (T + a.min_tiles - 1) / a.min_tiles);
+    }
     return max((int64_t)1, min(C, T));
 }
 
