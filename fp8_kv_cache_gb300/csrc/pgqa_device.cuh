@@ -355,13 +355,24 @@ struct WarpRing {
 //   P^T -> P      two movmatrix transposes turn the probabilities of the C
 //                 fragment into the B fragment of the next product;
 //   O^T += V^T P^T and l += 1^T P^T   m16n8k16 over the 16 tokens.
-template <bool kE4M3>
+template <bool kE4M3, bool kQRegs = false>
 struct WarpCore {
     static constexpr int kKCh = kE4M3 ? 4 : 8;   // 16-byte chunks of a K row per lane
     static constexpr int kVCh = kE4M3 ? 2 : 4;   // 16-byte chunks of a V row per lane
 
     float acc[17][4];     // [0..15]: O^T fragments, [16]: denominators
     float m0, m1;         // running max of heads 2q, 2q+1, log2 domain
+    uint2 qf[kQRegs ? 16 : 1];   // the lane's Q fragments, when held in registers
+
+    // With kQRegs, copies the lane's Q fragments out of qs (after staging).
+    __device__ void load_q(const uint2* qs, int lane)
+    {
+        if constexpr (kQRegs) {
+#pragma unroll
+            for (int s = 0; s < 16; ++s)
+                qf[s] = qs[s * 32 + lane];
+        }
+    }
 
     // Head-dim index of element n (0..63) of the K-row chunks lane q holds
     // (logical chunk c = q + 4i is the 16 bytes at byte 16c of the row).
@@ -428,7 +439,11 @@ struct WarpCore {
 #pragma unroll
             for (int w = 0; w < (kE4M3 ? 4 : 2); ++w) {
                 const int s = kE4M3 ? 4 * i + w : 2 * i + w;
-                const uint2 b = qs[s * 32 + lane];
+                uint2 b;
+                if constexpr (kQRegs)
+                    b = qf[s];
+                else
+                    b = qs[s * 32 + lane];
                 uint32_t a0, a1, a2, a3;
                 if (kE4M3) {
                     e4m3x4_to_f16x2x2(word(k0, w), a0, a2);
@@ -518,8 +533,8 @@ struct WarpCore {
 // k is half-tiles 2k and 2k+1; offset(h) returns, on lanes t < 8, the byte
 // offset of token t of half-tile h (or -1), and -1 on the other lanes.  The
 // ring keeps kNS half-tiles committed ahead of the tile being computed.
-template <bool kE4M3, int kNS, class Offset>
-__device__ __forceinline__ void run_tiles(WarpCore<kE4M3>& wc, WarpRing<kE4M3, kNS>& rg,
+template <bool kE4M3, int kNS, class Offset, bool kQRegs = false>
+__device__ __forceinline__ void run_tiles(WarpCore<kE4M3, kQRegs>& wc, WarpRing<kE4M3, kNS>& rg,
                                           const uint2* qs, const unsigned char* kb,
                                           const unsigned char* vb, int first, int end, int stride,
                                           int G, float scale_log2, int lane, Offset offset)
@@ -606,8 +621,8 @@ struct CtaSmem {
     }
 };
 
-template <bool kE4M3>
-__device__ void cta_merge(MergeSmem& sm, const WarpCore<kE4M3>& wc, int G, float v_scale,
+template <bool kE4M3, bool kQRegs = false>
+__device__ void cta_merge(MergeSmem& sm, const WarpCore<kE4M3, kQRegs>& wc, int G, float v_scale,
                           __half* out_rows, float* slot)
 {
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;

@@ -48,13 +48,15 @@ __global__ void __launch_bounds__(kThreads, kMinCtas<kE4M3>()) sparse_prefill_ke
     const int own = p >> 2;
     const int32_t* sel_row = a.sel + (size_t)r * a.n_sel;
 
-    using Core = WarpCore<kE4M3>;
+    // FP16 rows leave registers to spare: the Q fragments stay in registers.
+    using Core = WarpCore<kE4M3, !kE4M3>;
     const CtaSmem<kE4M3> cs = CtaSmem<kE4M3>::carve(smem_raw, w);
     WarpRing<kE4M3, kStages<kE4M3>()> rg;
     rg.init(cs.ring, cs.masks);
     Core::stage_q(cs.qs, a.q + ((size_t)r * a.Hq + (size_t)j * a.G) * kD, a.G, lane, w);
     Core wc;
     wc.reset();
+    bool q_loaded = false;
     // Chunks of block entries (selected blocks, then the tail entry): the CTA
     // resolves a chunk's entries (selection index -> block -> page) into the
     // address table first, so the ring fills need no dependent global load.
@@ -70,6 +72,10 @@ __global__ void __launch_bounds__(kThreads, kMinCtas<kE4M3>()) sparse_prefill_ke
             tab[e - e0] = make_int2(first, page);
         }
         __syncthreads();
+        if (!q_loaded) {
+            wc.load_q(cs.qs, lane);                  // Q staged before the first chunk's barrier
+            q_loaded = true;
+        }
         // half-tile h = block entries 2h, 2h+1 (8 tokens); lane t < 8 takes token t
         auto offset = [&](int h) -> int64_t {
             if (lane < kHalf) {
@@ -85,11 +91,11 @@ __global__ void __launch_bounds__(kThreads, kMinCtas<kE4M3>()) sparse_prefill_ke
             }
             return -1;
         };
-        run_tiles<kE4M3, kStages<kE4M3>()>(wc, rg, cs.qs, a.kv.k, a.kv.v, e0 / 4 + w,
-                                           (e1 + 3) / 4, kWarps, a.G, a.scale_log2, lane,
-                                           offset);
+        run_tiles<kE4M3, kStages<kE4M3>(), decltype(offset), !kE4M3>(
+            wc, rg, cs.qs, a.kv.k, a.kv.v, e0 / 4 + w, (e1 + 3) / 4, kWarps, a.G, a.scale_log2,
+            lane, offset);
     }
-    cta_merge<kE4M3>(*cs.merge, wc, a.G, a.v_scale, out_rows, nullptr);
+    cta_merge<kE4M3, !kE4M3>(*cs.merge, wc, a.G, a.v_scale, out_rows, nullptr);
     raise_flag(a.err, flags);
 }
 
