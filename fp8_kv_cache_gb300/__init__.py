@@ -27,6 +27,7 @@ __all__ = [
     "PagedGQAError", "library_path", "lib", "KV_FP16", "KV_E4M3",
     "FLAG_BAD_PAGE", "FLAG_SEQ_CLAMPED", "FLAG_EMPTY_ROW", "FLAG_QPOS_CLAMPED", "FLAG_BAD_SEL",
     "paged_gqa_decode", "paged_gqa_decode_noalloc", "paged_gqa_sparse_prefill",
+    "paged_gqa_sparse_prefill_route", "PREFILL_AUTO", "PREFILL_ROWWISE", "PREFILL_GROUPED",
     "paged_gqa_gather_dequant",
     "paged_gqa_sparse_prefill_tokens", "paged_gqa_decode_workspace_size",
     "paged_gqa_decode_workspace_size_splits",
@@ -45,6 +46,7 @@ FLAG_QPOS_CLAMPED = 8
 FLAG_BAD_SEL = 16
 FLAG_SCORES_SHORT = 32
 FLAG_BAD_LOGIT = 64
+FLAG_TIMEOUT = 128
 
 
 class PagedGQAError(RuntimeError):
@@ -100,6 +102,10 @@ def lib():
                                                    vp, i32, vp, i32, i32, i32, i32, i32, f32, f32,
                                                    vp, vp, vp]
             L.paged_gqa_sparse_prefill.restype = i32
+            L.paged_gqa_sparse_prefill_route.argtypes = [vp, vp, vp, KVLayout, i32, vp, i32, i32,
+                                                         vp, i32, vp, i32, i32, i32, i32, i32,
+                                                         f32, f32, vp, vp, vp, i32, i32]
+            L.paged_gqa_sparse_prefill_route.restype = i32
             L.paged_gqa_gather_dequant.argtypes = [vp, KVLayout, i32, vp, i64, vp, i32, i32, i32,
                                                    i32, i32, i32, i32, f32, vp, vp]
             L.paged_gqa_gather_dequant.restype = i32
@@ -240,11 +246,35 @@ def paged_gqa_decode_noalloc(q, k_cache, v_cache, block_table, seq_lens, page_si
     return out
 
 
+PREFILL_AUTO, PREFILL_ROWWISE, PREFILL_GROUPED = 0, 1, 2
+
+
 def paged_gqa_sparse_prefill(q, k_cache, v_cache, block_table, kv_len, sel_idx, q_pos, page_size,
                              softmax_scale, kv_scale=1.0, out=None, *, num_pages=None,
                              err_flag=None, stream=None):
     """Selected-sparse prefill of one sequence.  q [R, Hq, 256] float16;
     sel_idx int32 [R, n_sel] four-token block ids; q_pos int32 [R]."""
+    args, out = _prefill_args(q, k_cache, v_cache, block_table, kv_len, sel_idx, q_pos,
+                              page_size, softmax_scale, kv_scale, out, num_pages, err_flag, stream)
+    _check(lib().paged_gqa_sparse_prefill(*args), "paged_gqa_sparse_prefill")
+    return out
+
+
+def paged_gqa_sparse_prefill_route(q, k_cache, v_cache, block_table, kv_len, sel_idx, q_pos,
+                                   page_size, softmax_scale, kv_scale=1.0, out=None, *,
+                                   route=PREFILL_AUTO, rows_per_group=0, num_pages=None,
+                                   err_flag=None, stream=None):
+    """paged_gqa_sparse_prefill on a chosen kernel route (PREFILL_ROWWISE or
+    PREFILL_GROUPED; rows_per_group 0 = automatic group size)."""
+    args, out = _prefill_args(q, k_cache, v_cache, block_table, kv_len, sel_idx, q_pos,
+                              page_size, softmax_scale, kv_scale, out, num_pages, err_flag, stream)
+    _check(lib().paged_gqa_sparse_prefill_route(*args, int(route), int(rows_per_group)),
+           "paged_gqa_sparse_prefill_route")
+    return out
+
+
+def _prefill_args(q, k_cache, v_cache, block_table, kv_len, sel_idx, q_pos, page_size,
+                  softmax_scale, kv_scale, out, num_pages, err_flag, stream):
     torch = _torch()
     R, Hq, D = q.shape
     Hkv = k_cache.shape[2]
@@ -253,13 +283,11 @@ def paged_gqa_sparse_prefill(q, k_cache, v_cache, block_table, kv_len, sel_idx, 
     if num_pages is None:
         num_pages = k_cache.shape[0]
     n_sel = sel_idx.shape[1] if sel_idx.dim() == 2 else 0
-    st = lib().paged_gqa_sparse_prefill(
-        _ptr(q), _ptr(k_cache), _ptr(v_cache), _layout(k_cache, v_cache), _kv_dtype(k_cache),
-        _ptr(block_table), num_pages, kv_len, _ptr(sel_idx) if n_sel else None, n_sel,
-        _ptr(q_pos), R, Hq, Hkv, D, page_size, float(kv_scale), float(softmax_scale),
-        _ptr(out), _ptr(err_flag), _stream(stream))
-    _check(st, "paged_gqa_sparse_prefill")
-    return out
+    return (_ptr(q), _ptr(k_cache), _ptr(v_cache), _layout(k_cache, v_cache),
+            _kv_dtype(k_cache), _ptr(block_table), num_pages, kv_len,
+            _ptr(sel_idx) if n_sel else None, n_sel, _ptr(q_pos), R, Hq, Hkv, D, page_size,
+            float(kv_scale), float(softmax_scale), _ptr(out), _ptr(err_flag),
+            _stream(stream)), out
 
 
 def paged_gqa_gather_dequant(cache, block_table, seq_lens, page_size, max_seq_len, kv_scale=1.0,

@@ -21,7 +21,7 @@ INCLUDE = os.path.join(os.path.dirname(PKG), "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIBRARY = os.path.join(PKG, "libpaged_gqa.so")
 SOURCES = ["api.cu", "decode.cu", "prefill.cu", "inspect.cu", "select.cu", "sample_mask.cu",
-           "decode_noalloc.cu"]
+           "decode_noalloc.cu", "prefill_grouped.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

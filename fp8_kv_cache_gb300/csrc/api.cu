@@ -224,6 +224,23 @@ int paged_gqa_sparse_prefill(const void* q, const void* k_cache, const void* v_c
                              int Hq, int Hkv, int D, int page_size, float kv_scale,
                              float softmax_scale, void* out, int* err_flag, void* stream)
 {
+    return paged_gqa_sparse_prefill_route(q, k_cache, v_cache, kv_layout, kv_dtype, block_table,
+                                          num_pages, kv_len, sel_idx, n_sel, q_pos, R, Hq, Hkv,
+                                          D, page_size, kv_scale, softmax_scale, out, err_flag,
+                                          stream, PAGED_GQA_PREFILL_AUTO, 0);
+}
+
+int paged_gqa_sparse_prefill_route(const void* q, const void* k_cache, const void* v_cache,
+                                   paged_gqa_kv_layout kv_layout, int kv_dtype,
+                                   const int32_t* block_table, int num_pages, int kv_len,
+                                   const int32_t* sel_idx, int n_sel, const int32_t* q_pos,
+                                   int R, int Hq, int Hkv, int D, int page_size, float kv_scale,
+                                   float softmax_scale, void* out, int* err_flag, void* stream,
+                                   int route, int rows_per_group)
+{
+    if (route < PAGED_GQA_PREFILL_AUTO || route > PAGED_GQA_PREFILL_GROUPED ||
+        rows_per_group < 0)
+        return PAGED_GQA_ERR_SHAPE;
     if (R < 0 || n_sel < 0 || Hq < 1 || Hkv < 1 || kv_len < 0 || Hq % Hkv != 0)
         return PAGED_GQA_ERR_SHAPE;
     if (D != kD || Hq / Hkv > kGMax)
@@ -259,7 +276,17 @@ int paged_gqa_sparse_prefill(const void* q, const void* k_cache, const void* v_c
     a.v_scale = e4m3 ? kv_scale : 1.f;
     a.out = static_cast<__half*>(out);
     a.err = err_flag;
-    const cudaError_t e = launch_prefill(a, e4m3, static_cast<cudaStream_t>(stream));
+    const bool grouped_ok = grouped_prefill_supported(a, e4m3);
+    if (route == PAGED_GQA_PREFILL_GROUPED && !grouped_ok)
+        return PAGED_GQA_ERR_UNSUPPORTED;
+    if (rows_per_group > kGroupSlots / a.G)
+        return PAGED_GQA_ERR_SHAPE;
+    // The automatic choice is the per-row kernel: on the 4096-row workload it
+    // runs at the gather ceiling, ahead of the grouped kernel.
+    const bool grouped = route == PAGED_GQA_PREFILL_GROUPED;
+    const cudaError_t e =
+        grouped ? launch_prefill_grouped(a, rows_per_group, static_cast<cudaStream_t>(stream))
+                : launch_prefill(a, e4m3, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PAGED_GQA_OK : PAGED_GQA_ERR_CUDA;
 }
 

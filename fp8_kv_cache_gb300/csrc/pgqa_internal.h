@@ -55,6 +55,18 @@ struct PrefillArgs {
     int* err;
 };
 
+// Grouped sparse prefill (prefill_grouped.cu): a union bitmap over the
+// sequence's four-token blocks of at most kGroupMaxWords words.
+constexpr int kGroupMaxWords = 1024;
+constexpr int kGroupSlots = 128;      // query-head slots of a group: the M of one MMA
+
+struct GroupArgs {
+    PrefillArgs a;
+    int Rg;              // query rows per group (unit = group x KV head)
+    int n_units;
+    int nbw;             // words of the union bitmap
+};
+
 struct SelectArgs {
     const float* scores;
     int64_t stride;
@@ -83,6 +95,9 @@ int split_ctas_per_sm(bool e4m3);
 
 cudaError_t launch_decode(const DecodeArgs& a, bool e4m3, cudaStream_t s, void* ev0, void* ev1);
 cudaError_t launch_prefill(const PrefillArgs& a, bool e4m3, cudaStream_t s);
+bool grouped_prefill_supported(const PrefillArgs& a, bool e4m3);
+int grouped_prefill_rows(const PrefillArgs& a, int sms, int rows_per_group);
+cudaError_t launch_prefill_grouped(const PrefillArgs& a, int rows_per_group, cudaStream_t s);
 cudaError_t launch_gather(const KVGeom& g, bool e4m3, const int32_t* bt, int64_t bt_stride,
                           const int32_t* seq_lens, int B, int T, int Hkv, int max_seq_len,
                           float kv_scale, float* out, cudaStream_t s);

@@ -1,0 +1,727 @@
+// prefill_grouped.cu -- selected-sparse paged prefill with grouped query rows
+// on the fifth-generation tensor cores (FP16 KV).
+//
+// Operation: "[Kernel][SM70] Accelerate Qwen3.8 QSA paged prefill"
+// (1Cat-vLLM #378), Changes: query row r with p = min(q_pos[r], kv_len - 1)
+// attends to its selected four-token blocks strictly before its own block,
+// then to its own block up to p, read in place from the paged cache;
+// padding, non-causal selections and invalid pages are inert.
+//
+// Design (ours, GB300-first).  The per-row kernel of prefill.cu reads each
+// row's ~2050 tokens on its own: at 4096 rows that is 8.6 GB pulled from L2
+// for a 32 MiB cache, and the gather, not the arithmetic, bounds it.  Nearby
+// rows select many of the same blocks, so here one CTA owns a group of
+// consecutive rows of one KV head -- up to 128 query-head slots, the M of one
+// tcgen05 MMA -- and streams the UNION of their blocks once:
+//   * setup: the rows' valid entries are OR-ed into a bitmap over the
+//     sequence's blocks; a prefix popcount ranks the union; each row gets a
+//     16-bit mask per 64-token stage saying which of the stage's 16 blocks it
+//     attends (its own block limited to positions <= p).
+//   * 8 producer warps gather stage after stage (K of half-tile m+1, then V
+//     of m) with 16-byte cp.async into a 4-stage ring, laid out as the
+//     128-byte-swizzled K-major tile (see tc_device.cuh).
+//   * one thread issues S = Q K^T (M = 128 slots, N = 64 tokens, K = 256;
+//     Q and K from shared memory) into a TMEM buffer, and O += P V (M = 128,
+//     N = 256, K = 64; P from TMEM, V from the same ring bytes as an MN-major
+//     operand) into a 256-column TMEM accumulator.
+//   * 4 softmax warps own one slot each per thread: they read the slot's 64
+//     scores from TMEM, mask them, keep the running max and sum, write the
+//     FP16 probabilities back over the scores (two S/P buffers alternate), and
+//     rescale O in TMEM only when a running max grows by more than 2^8 (the
+//     sum and O always share one reference max, so the result is exact up to
+//     rounding).
+// Masked-out (slot, token) pairs cost tensor-core work but no memory traffic;
+// on the 4096-row workload the union is about 0.6 of the per-row gather.
+// Groups are sized so the units fill whole waves of one CTA per SM and are
+// dealt in snake order (later rows have longer prefixes).
+//
+// Duplicated selections (a caller error) keep their meaning -- a block listed
+// c times counts c times -- through a slow per-row recount.
+#include <algorithm>
+#include <atomic>
+
+#include "pgqa_internal.h"
+#include "tc_device.cuh"
+
+namespace pgqa {
+namespace grp {
+
+constexpr int kM = kGroupSlots;               // query-head slots of a group (MMA M)
+constexpr int kStageTokens = 64;             // tokens per stage: 16 four-token blocks
+constexpr int kStageBlocks = 16;
+constexpr int kNS = 5;                       // ring stages, one producer warp each
+constexpr int kRegionBytes = kStageTokens * 128;      // 64 head-dim columns of a stage
+constexpr int kStageBytes = kStageTokens * kD * 2;    // 32 KB
+constexpr int kMaskWords = 4096;             // 16 KB of per-row stage masks
+constexpr int kSoftWarps = 8, kMmaWarp = 8, kProdWarps = kNS, kProdWarp0 = 9;
+constexpr int kThreads = 32 * (kSoftWarps + 1 + kProdWarps);
+constexpr float kRescaleSlack = 8.f;         // log2-domain growth tolerated before rescaling O
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemQ = 0;               // Q: 128 columns of f16 pairs
+constexpr uint32_t kTmemS = 128;             // S buffers at 128 and 192 (64 columns each)
+constexpr uint32_t kTmemO = 256;             // O: 256 f32 columns
+constexpr int kPBytes = kM * 128;            // one P buffer: 128 slots x 64 tokens, K-major
+
+struct Smem {
+    unsigned char ring[kNS][kStageBytes];
+    unsigned char p[2][kPBytes];             // FP16 probabilities, the A operand of P V
+    uint32_t bitmap[kGroupMaxWords];         // union of the group's blocks
+    int rank[kGroupMaxWords];                // exclusive prefix popcount of bitmap
+    uint32_t masks[kMaskWords];              // [row][stage / 2]: two 16-bit stage masks per word
+    int row_p[kM], row_own[kM], row_rank_own[kM], row_dup[kM];
+    float xm[2][2][kM];                      // [stage parity][half][slot]: stage maxima exchanged
+    float xl[2][kM];                         // [half][slot]: final sums exchanged
+    uint64_t full[kNS], empty[kNS];
+    uint64_t s_full[2], s_free[2], p_full[2], p_free[2], done;
+    uint32_t tmem_base;
+    int flags, n_union, abort;
+};
+
+constexpr size_t kSmemBytes = sizeof(Smem) + 1024;   // + alignment of the tiles
+
+// Where a unit's loop stands; every role walks the same sequence, so the
+// global counters agree between roles without communication.
+struct Cursor {
+    uint32_t it = 0;    // ring stage counter
+    uint32_t g = 0;     // half-tile (S/P buffer) counter
+};
+
+// Bounded wait; after any wait of the CTA has timed out, waits are skipped
+// (every role keeps its control flow, so all barriers are still reached and
+// the kernel ends; the result is then garbage and PAGED_GQA_FLAG_TIMEOUT set).
+__device__ __forceinline__ void wait_or_abort(Smem& sm, uint64_t* bar, uint32_t par)
+{
+    volatile int* ab = &sm.abort;
+    if (*ab)
+        return;
+    if (!tc::mbar_wait(bar, par))
+        *ab = 1;
+}
+
+__device__ __forceinline__ bool page_valid_block(const KVGeom& g, const int32_t* bt, int b,
+                                                 int& page, int& slot)
+{
+    int pi;
+    page_and_slot(g, 4 * b, pi, slot);
+    page = __ldg(bt + pi);
+    return page >= 0 && page < g.num_pages;
+}
+
+// Block of entry e of group row rl (selected blocks, then the own block), or
+// -1 when the entry is not attended; adds the entry's flags.
+__device__ __forceinline__ int entry_block(const GroupArgs& ga, const Smem& sm, int r0, int rl,
+                                           int e, int& flags)
+{
+    const PrefillArgs& a = ga.a;
+    const int own = sm.row_own[rl];
+    if (own < 0)
+        return -1;
+    int b;
+    if (e < a.n_sel) {
+        b = __ldg(a.sel + (size_t)(r0 + rl) * a.n_sel + e);
+        if (b < 0)
+            return -1;
+        if (b >= own) {
+            flags |= PAGED_GQA_FLAG_BAD_SEL;
+            return -1;
+        }
+    } else {
+        b = own;
+    }
+    int page, slot;
+    if (!page_valid_block(a.kv, a.bt, b, page, slot)) {
+        flags |= PAGED_GQA_FLAG_BAD_PAGE;
+        return -1;
+    }
+    return b;
+}
+
+__device__ __forceinline__ int rank_of_block(const Smem& sm, int b)
+{
+    const int w = b >> 5;
+    return sm.rank[w] + __popc(sm.bitmap[w] & ((1u << (b & 31)) - 1u));
+}
+
+// The union block of rank k (k < n_union).
+__device__ __forceinline__ int block_of_rank(const Smem& sm, int nbw, int k)
+{
+    int lo = 0, hi = nbw - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (sm.rank[mid] <= k)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    return 32 * lo + (int)__fns(sm.bitmap[lo], 0, k - sm.rank[lo] + 1);
+}
+
+// Stage masks of the half-tiles [ht0, ht0 + cap) for every row of the group,
+// built by the 128 softmax threads (named barrier 1).  A block already
+// present in a row's mask is a duplicated selection: the row is marked.
+__device__ void build_masks(const GroupArgs& ga, Smem& sm, int r0, int Rg, int ht0, int cap,
+                            int words_per_row)
+{
+    const int t = threadIdx.x;
+    asm volatile("bar.sync 1, %0;" ::"n"(kSoftWarps * 32) : "memory");   // old masks read
+    for (int i = t; i < Rg * words_per_row; i += kSoftWarps * 32)
+        sm.masks[i] = 0u;
+    asm volatile("bar.sync 1, %0;" ::"n"(kSoftWarps * 32) : "memory");
+    const int n_ent = ga.a.n_sel + 1;
+    int flags = 0;
+    for (int idx = t; idx < Rg * n_ent; idx += kSoftWarps * 32) {
+        const int rl = idx / n_ent, e = idx - rl * n_ent;
+        const int b = entry_block(ga, sm, r0, rl, e, flags);
+        if (b < 0)
+            continue;
+        const int k = rank_of_block(sm, b), ht = (k >> 4) - ht0;
+        if (ht < 0 || ht >= cap)
+            continue;
+        const uint32_t bit = 1u << (((ht & 1) << 4) + (k & 15));
+        const uint32_t old = atomicOr(&sm.masks[rl * words_per_row + (ht >> 1)], bit);
+        if (old & bit)
+            sm.row_dup[rl] = 1;
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(kSoftWarps * 32) : "memory");
+}
+
+// Everything a unit needs before its first stage: row positions, the union
+// bitmap and its ranks, the Q tile, the first window of masks.  All threads.
+__device__ void unit_setup(const GroupArgs& ga, Smem& sm, int r0, int Rg, int j, int nbw,
+                           int words_per_row, int cap)
+{
+    const PrefillArgs& a = ga.a;
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        sm.flags = 0;
+        sm.n_union = 0;
+    }
+    if (tid < Rg) {
+        int p = __ldg(a.q_pos + r0 + tid), fl = 0, own = -1;
+        if (p < 0 || a.kv_len <= 0) {
+            fl |= PAGED_GQA_FLAG_EMPTY_ROW;
+        } else {
+            if (p >= a.kv_len) {
+                p = a.kv_len - 1;
+                fl |= PAGED_GQA_FLAG_QPOS_CLAMPED;
+            }
+            own = p >> 2;
+        }
+        sm.row_p[tid] = p;
+        sm.row_own[tid] = own;
+        sm.row_rank_own[tid] = -1;
+        sm.row_dup[tid] = 0;
+        if (fl)
+            atomicOr(&sm.flags, fl);
+    }
+    for (int w = tid; w < nbw; w += kThreads)
+        sm.bitmap[w] = 0u;
+    __syncthreads();
+
+    const int n_ent = a.n_sel + 1;
+    int flags = 0;
+    for (int idx = tid; idx < Rg * n_ent; idx += kThreads) {
+        const int rl = idx / n_ent, e = idx - rl * n_ent;
+        const int b = entry_block(ga, sm, r0, rl, e, flags);
+        if (b >= 0)
+            atomicOr(&sm.bitmap[b >> 5], 1u << (b & 31));
+    }
+    if (flags)
+        atomicOr(&sm.flags, flags);
+    __syncthreads();
+
+    if (tid < 32) {                          // exclusive scan of the word popcounts
+        const int per = (nbw + 31) >> 5, w0 = tid * per, w1 = min(nbw, w0 + per);
+        int sum = 0;
+        for (int w = w0; w < w1; ++w)
+            sum += __popc(sm.bitmap[w]);
+        int inc = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, inc, o);
+            if (tid >= o)
+                inc += v;
+        }
+        int run = inc - sum;
+        for (int w = w0; w < w1; ++w) {
+            sm.rank[w] = run;
+            run += __popc(sm.bitmap[w]);
+        }
+        if (tid == 31)
+            sm.n_union = inc;
+    }
+    __syncthreads();
+
+    if (tid < Rg) {
+        const int own = sm.row_own[tid];
+        if (own >= 0 && ((sm.bitmap[own >> 5] >> (own & 31)) & 1u))
+            sm.row_rank_own[tid] = rank_of_block(sm, own);
+    }
+    if (tid < kSoftWarps * 32) {             // Q into TMEM: lane = slot = (row slot / G, head slot % G)
+        const int slot = tid & (kM - 1), half = tid >> 7;         // two threads per slot
+        const int rl = slot / a.G, h = slot - rl * a.G;
+        const bool live = rl < Rg && sm.row_own[rl] >= 0;
+        const uint4* src = reinterpret_cast<const uint4*>(
+            a.q + ((size_t)(r0 + (live ? rl : 0)) * a.Hq + (size_t)j * a.G + (live ? h : 0)) * kD);
+        const uint32_t tl = sm.tmem_base + ((uint32_t)(32 * ((tid >> 5) & 3)) << 16);
+#pragma unroll 1
+        for (int part = 0; part < 2; ++part) {   // 8 chunks of 16 bytes = 32 columns of f16 pairs
+            uint32_t w[32];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const uint4 v = live ? __ldg(src + 16 * half + 8 * part + c) : make_uint4(0u, 0u, 0u, 0u);
+                w[4 * c] = v.x;
+                w[4 * c + 1] = v.y;
+                w[4 * c + 2] = v.z;
+                w[4 * c + 3] = v.w;
+            }
+            tc::tmem_st32(tl + kTmemQ + 64 * half + 32 * part, w);
+        }
+        tc::tmem_wait_st();
+        build_masks(ga, sm, r0, Rg, 0, cap, words_per_row);
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+}
+
+// Stage q of a unit with nt half-tiles.  The order is K0, K1, K2, V0, K3,
+// V1, ..., K(nt-1), V(nt-4), V(nt-3), V(nt-2), V(nt-1): Q K^T runs two
+// half-tiles ahead of P V, so the next scores are ready while the softmax of
+// the current half-tile and its P V run.
+__device__ __forceinline__ void stage_of(int q, int nt, bool& is_v, int& ht)
+{
+    const int lead = nt < 3 ? nt : 3;
+    if (q < lead) {
+        is_v = false;
+        ht = q;
+        return;
+    }
+    const int r = q - lead, pairs = 2 * (nt - lead);
+    if (r < pairs) {
+        is_v = (r & 1) == 0;
+        ht = is_v ? r >> 1 : (r >> 1) + 3;
+    } else {
+        is_v = true;
+        ht = r - pairs + (nt - lead);
+    }
+}
+
+// Producer warps: warp pw owns ring slot pw and fills every stage that lands
+// there (stages it with it % kNS == pw): lanes 0..15 resolve the stage's 16
+// blocks (rank -> block -> page) in parallel, then each lane copies its
+// 16-byte chunk of all 64 rows.  The warp waits for its own copies, fences
+// them for the tensor cores and publishes the stage; stages of different
+// warps are in flight together.
+__device__ void produce(const GroupArgs& ga, Smem& sm, Cursor& cur, int j, int nbw, int nt,
+                        int n_union)
+{
+    const PrefillArgs& a = ga.a;
+    const int lane = threadIdx.x & 31, pw = (threadIdx.x >> 5) - kProdWarp0;
+    for (int q = 0; q < 2 * nt; ++q, ++cur.it) {
+        const int s = cur.it % kNS;
+        if (s != pw)
+            continue;
+        bool is_v;
+        int ht;
+        stage_of(q, nt, is_v, ht);
+        if (cur.it >= (uint32_t)kNS)
+            wait_or_abort(sm, &sm.empty[s], ((cur.it / kNS) - 1) & 1);
+        int64_t off = -1;
+        if (lane < kStageBlocks) {
+            const int k = kStageBlocks * ht + lane;
+            if (k < n_union) {
+                const int b = block_of_rank(sm, nbw, k);
+                int page, slot;
+                page_valid_block(a.kv, a.bt, b, page, slot);
+                off = row_offset(a.kv, page, slot, j);
+            }
+        }
+        const unsigned char* base = is_v ? a.kv.v : a.kv.k;
+        const uint32_t st = tc::smem_addr(sm.ring[s]) + (lane >> 3) * kRegionBytes;
+        const uint32_t x = lane & 7;
+#pragma unroll 4
+        for (int blk = 0; blk < kStageBlocks; ++blk) {
+            const int64_t o = __shfl_sync(0xffffffffu, off, blk);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int row = 4 * blk + u;
+                const uint32_t dst = st + row * 128 + ((x ^ (row & 7)) << 4);
+                const unsigned char* src = base + (o < 0 ? 0 : o + u * a.kv.token_b + 16 * lane);
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                             "r"(o < 0 ? 0 : 16)
+                             : "memory");
+            }
+        }
+        cp_async_commit();
+        cp_async_wait<0>();
+        tc::fence_async_shared();
+        tc::mbar_arrive(&sm.full[s]);
+    }
+}
+
+// The MMA thread, in stage order: Q K^T of half-tile m+2 goes out as soon as
+// the softmax has read S(m), before P V of m.
+__device__ void issue_mma(Smem& sm, Cursor& cur, int nt)
+{
+    constexpr uint32_t kIdQK = tc::f16_idesc(kM, kStageTokens, false, false);
+    constexpr uint32_t kIdPV = tc::f16_idesc(kM, kD, false, true);
+    const uint32_t tm = sm.tmem_base;
+    const uint32_t g0 = cur.g;
+    for (int q = 0; q < 2 * nt; ++q, ++cur.it) {
+        bool is_v;
+        int ht;
+        stage_of(q, nt, is_v, ht);
+        const uint32_t g = g0 + ht, buf = g & 1, s = cur.it % kNS;
+        const uint32_t st = tc::smem_addr(sm.ring[s]);
+        wait_or_abort(sm, &sm.full[s], (cur.it / kNS) & 1);
+        if (!is_v) {
+            if (g >= 2)
+                wait_or_abort(sm, &sm.s_free[buf], ((g >> 1) - 1) & 1);
+            tc::fence_after_sync();
+#pragma unroll
+            for (int kk = 0; kk < kD / 16; ++kk) {
+                const uint32_t off = (kk & 3) * 32;
+                const uint64_t db = tc::sw128_desc(st + (kk >> 2) * kRegionBytes + off, 16, 1024);
+                tc::mma_ts(tm + kTmemS + 64 * buf, tm + kTmemQ + 8 * kk, db, kIdQK, kk > 0);
+            }
+            tc::mma_commit(&sm.empty[s]);
+            tc::mma_commit(&sm.s_full[buf]);
+        } else {
+            wait_or_abort(sm, &sm.p_full[buf], (g >> 1) & 1);
+            tc::fence_after_sync();
+            const uint32_t pa = tc::smem_addr(sm.p[buf]);
+#pragma unroll
+            for (int kk = 0; kk < kStageTokens / 16; ++kk) {
+                const uint64_t da = tc::sw128_desc(pa + kk * 32, 16, 1024);
+                const uint64_t db = tc::sw128_desc(st + kk * 2048, kRegionBytes, 1024);
+                tc::mma_ss(tm + kTmemO, da, db, kIdPV, (ht > 0 || kk > 0));
+            }
+            tc::mma_commit(&sm.empty[s]);
+            tc::mma_commit(&sm.p_free[buf]);
+        }
+    }
+    cur.g = g0 + nt;
+}
+
+// How many times block b is listed in the selection row (duplicates are a
+// caller error that still counts per listing); the own block counts once.
+__device__ int listed_count(const PrefillArgs& a, int r, int b, int own)
+{
+    if (b == own)
+        return 1;
+    const int32_t* row = a.sel + (size_t)r * a.n_sel;
+    int c = 0;
+    for (int e = 0; e < a.n_sel; ++e)
+        c += __ldg(row + e) == b;
+    return c;
+}
+
+// Named barrier of the two softmax warps that share TMEM lane quarter wq.
+__device__ __forceinline__ void pair_sync(int wq)
+{
+    asm volatile("bar.sync %0, 64;" ::"r"(2 + wq) : "memory");
+}
+
+// Softmax warps: slot = t & 127 (row slot / G, head slot % G) = TMEM lane;
+// half = t >> 7 takes score columns 32 half .. 32 half + 31 of each stage (the
+// warps of both halves on one lane quarter exchange the stage maximum through
+// shared memory), O columns 128 half .. 128 half + 127 when O is rescaled or
+// written, and writes P columns 16 half .. 16 half + 15.
+__device__ void softmax_unit(const GroupArgs& ga, Smem& sm, Cursor& cur, int r0, int Rg, int j,
+                             int nt, int nbw, int cap, int words_per_row)
+{
+    const PrefillArgs& a = ga.a;
+    const int t = threadIdx.x, half = t >> 7, slot = t & (kM - 1), wq = (t >> 5) & 3;
+    const int rl = slot / a.G, h = slot - rl * a.G;
+    const bool slot_ok = rl < Rg;
+    const int own = slot_ok ? sm.row_own[rl] : -1;
+    const int rank_own = slot_ok ? sm.row_rank_own[rl] : -1;
+    const int tail_n = own >= 0 ? sm.row_p[rl] - 4 * own + 1 : 0;
+    const uint32_t tl = sm.tmem_base + ((uint32_t)(32 * wq) << 16);
+    const float sl2 = a.scale_log2;
+    float m_ref = -INFINITY, l = 0.f;
+    const uint32_t g0 = cur.g;
+    int ht0 = 0;
+    for (int i = 0; i < nt; ++i) {
+        const uint32_t g = g0 + i, buf = g & 1;
+        if (i - ht0 == cap) {
+            ht0 = i;
+            build_masks(ga, sm, r0, Rg, ht0, cap, words_per_row);
+        }
+        // live bits of this thread's 32 tokens (8 blocks of 4)
+        uint32_t live = 0u;
+        if (own >= 0) {
+            const int li = i - ht0;
+            const uint32_t m8 =
+                (sm.masks[rl * words_per_row + (li >> 1)] >> (((li & 1) << 4) + 8 * half)) & 0xFFu;
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                live |= ((m8 >> k) & 1u) ? (0xFu << (4 * k)) : 0u;
+            if (rank_own >= 0 && (rank_own >> 4) == i) {
+                const int ko = (rank_own & 15) - 8 * half;
+                if (ko >= 0 && ko < 8)
+                    live &= ~((0xFu & ~((1u << tail_n) - 1u)) << (4 * ko));
+            }
+        }
+        const bool dup = own >= 0 && sm.row_dup[rl] != 0;
+
+        wait_or_abort(sm, &sm.s_full[buf], (g >> 1) & 1);
+        tc::fence_after_sync();
+        uint32_t sv[32];
+        tc::tmem_ld32(tl + kTmemS + 64 * buf + 32 * half, sv);
+        tc::tmem_wait_ld();
+        tc::fence_before_sync();
+        tc::mbar_arrive(&sm.s_free[buf]);      // Q K^T of half-tile g + 2 may overwrite S
+        float x[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+            x[c] = ((live >> c) & 1u) ? __uint_as_float(sv[c]) * sl2 : -INFINITY;
+        float mx[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+            mx[c] = fmaxf(x[c], x[c + 16]);
+#pragma unroll
+        for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+            for (int c = 0; c < w; ++c)
+                mx[c] = fmaxf(mx[c], mx[c + w]);
+        // (double-buffered by stage parity: a half can only write the buffer
+        // again after both halves passed the next pair barrier)
+        sm.xm[i & 1][half][slot] = mx[0];
+        pair_sync(wq);
+        const float mt = fmaxf(mx[0], sm.xm[i & 1][half ^ 1][slot]);
+
+        bool resc = false;
+        float alpha = 1.f;
+        if (mt > m_ref + kRescaleSlack) {
+            alpha = ex2(m_ref - mt);             // 0 while nothing was attended yet
+            resc = m_ref != -INFINITY;
+            l *= alpha;
+            m_ref = mt;
+        }
+        if (__any_sync(0xffffffffu, resc)) {
+            // O still holds the sum under the old reference: wait for P V of
+            // the previous half-tile (P V before it on that buffer was waited
+            // for before P(g-1) was written; P V completes in issue order),
+            // then scale this thread's half of the lane's O row in place.
+            wait_or_abort(sm, &sm.p_free[(g - 1) & 1], ((g - 1) >> 1) & 1);
+            tc::fence_after_sync();
+            const float f = resc ? alpha : 1.f;
+#pragma unroll 1
+            for (int c = 0; c < kD / 64; ++c) {
+                uint32_t o[32];
+                const uint32_t col = kTmemO + 128 * half + 32 * c;
+                tc::tmem_ld32(tl + col, o);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+                tc::tmem_st32(tl + col, o);
+            }
+        }
+
+        uint32_t pk[16];
+        float lsum = 0.f;
+#pragma unroll
+        for (int kb = 0; kb < 8; ++kb) {
+            float pv[4] = {0.f, 0.f, 0.f, 0.f};
+            if (__any_sync(0xffffffffu, (live >> (4 * kb)) & 0xFu)) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    pv[u] = x[4 * kb + u] == -INFINITY ? 0.f : ex2(x[4 * kb + u] - m_ref);
+                if (dup && ((live >> (4 * kb)) & 0xFu)) {
+                    const int blk = kStageBlocks * i + 8 * half + kb;
+                    const float cnt =
+                        (float)listed_count(a, r0 + rl, block_of_rank(sm, nbw, blk), own);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        pv[u] *= cnt;
+                }
+            }
+            const __half2 p01 = __floats2half2_rn(pv[0], pv[1]);
+            const __half2 p23 = __floats2half2_rn(pv[2], pv[3]);
+            const float2 f01 = __half22float2(p01), f23 = __half22float2(p23);
+            lsum += (f01.x + f01.y) + (f23.x + f23.y);
+            pk[2 * kb] = *reinterpret_cast<const uint32_t*>(&p01);
+            pk[2 * kb + 1] = *reinterpret_cast<const uint32_t*>(&p23);
+        }
+        l += lsum;
+        // P(g) goes to shared-memory buffer buf once P V of half-tile g - 2
+        // has consumed it: row = slot, this half's 32 tokens = chunks
+        // 4 half .. 4 half + 3 of the 128-byte row (128-byte swizzle).
+        if (g >= 2)
+            wait_or_abort(sm, &sm.p_free[buf], ((g >> 1) - 1) & 1);
+        unsigned char* prow = sm.p[buf] + slot * 128;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            *reinterpret_cast<uint4*>(prow + (((4 * half + c) ^ (slot & 7)) << 4)) =
+                make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        tc::fence_async_shared();
+        tc::tmem_wait_st();                    // O rescale stores, if any
+        tc::fence_before_sync();
+        tc::mbar_arrive(&sm.p_full[buf]);
+    }
+
+    // Epilogue: O / l as binary16 (a row with nothing attended is zero), once
+    // the last P V is done (the one before it on that buffer was waited for
+    // before its P was written, so one parity wait is unambiguous).
+    sm.xl[half][slot] = l;
+    pair_sync(wq);
+    const float lt = l + sm.xl[half ^ 1][slot];
+    if (nt > 0) {
+        const uint32_t g_last = g0 + nt - 1;
+        wait_or_abort(sm, &sm.p_free[g_last & 1], (g_last >> 1) & 1);
+        tc::fence_after_sync();
+    }
+    const float inv = lt > 0.f ? 1.f / lt : 0.f;
+    uint4* dst = slot_ok ? reinterpret_cast<uint4*>(
+                               a.out + ((size_t)(r0 + rl) * a.Hq + (size_t)j * a.G + h) * kD +
+                               128 * half)
+                         : nullptr;
+#pragma unroll 1
+    for (int c = 0; c < kD / 64; ++c) {
+        uint32_t o[32];
+        if (nt > 0) {
+            tc::tmem_ld32(tl + kTmemO + 128 * half + 32 * c, o);
+            tc::tmem_wait_ld();
+        }
+        if (dst != nullptr) {
+            uint32_t hv[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const float v0 = (nt > 0 && lt > 0.f) ? __uint_as_float(o[2 * e]) * inv : 0.f;
+                const float v1 = (nt > 0 && lt > 0.f) ? __uint_as_float(o[2 * e + 1]) * inv : 0.f;
+                hv[e] = pack_half2(v0, v1);
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                dst[4 * c + e] = make_uint4(hv[4 * e], hv[4 * e + 1], hv[4 * e + 2], hv[4 * e + 3]);
+        }
+    }
+    tc::fence_before_sync();
+    cur.g = g0 + nt;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) sparse_prefill_grouped_kernel(const GroupArgs ga)
+{
+    extern __shared__ unsigned char smem_raw[];
+    Smem& sm = *reinterpret_cast<Smem*>(
+        smem_raw + ((1024u - (tc::smem_addr(smem_raw) & 1023u)) & 1023u));
+    const PrefillArgs& a = ga.a;
+    const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+    if (tid == 0) {
+        for (int s = 0; s < kNS; ++s) {
+            tc::mbar_init(&sm.full[s], 32);
+            tc::mbar_init(&sm.empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            tc::mbar_init(&sm.s_full[b], 1);
+            tc::mbar_init(&sm.s_free[b], kSoftWarps * 32);
+            tc::mbar_init(&sm.p_full[b], kSoftWarps * 32);
+            tc::mbar_init(&sm.p_free[b], 1);
+        }
+        tc::mbar_init(&sm.done, 1);
+        sm.abort = 0;
+        tc::mbar_init_fence();
+    }
+    if (w == kMmaWarp)
+        tc::tmem_alloc(&sm.tmem_base, kTmemCols);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+
+    Cursor cur;
+    const int C = gridDim.x;
+    for (int wave = 0; wave * C < ga.n_units; ++wave) {
+        const int u = wave * C + ((wave & 1) ? C - 1 - (int)blockIdx.x : (int)blockIdx.x);
+        if (u >= ga.n_units)
+            continue;
+        const int gi = u / a.Hkv, j = u - gi * a.Hkv;
+        const int r0 = gi * ga.Rg, Rg = min(ga.Rg, a.R - r0);
+        const int words_per_row = kMaskWords / Rg, cap = 2 * words_per_row;
+        unit_setup(ga, sm, r0, Rg, j, ga.nbw, words_per_row, cap);
+        const int nt = (sm.n_union + kStageBlocks - 1) / kStageBlocks;
+        if (w >= kProdWarp0)
+            produce(ga, sm, cur, j, ga.nbw, nt, sm.n_union);
+        else if (w == kMmaWarp && lane == 0)
+            issue_mma(sm, cur, nt);
+        else if (w < kSoftWarps)
+            softmax_unit(ga, sm, cur, r0, Rg, j, nt, ga.nbw, cap, words_per_row);
+        if (tid == 0 && sm.flags)
+            raise_flag(a.err, sm.flags);
+        tc::fence_before_sync();
+        __syncthreads();
+        tc::fence_after_sync();
+    }
+    if (w == kMmaWarp && lane == 0) {        // every MMA done before TMEM is released
+        tc::mma_commit(&sm.done);
+        wait_or_abort(sm, &sm.done, 0);
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (tid == 0 && sm.abort)
+        raise_flag(a.err, PAGED_GQA_FLAG_TIMEOUT);
+    if (w == kMmaWarp)
+        tc::tmem_dealloc(sm.tmem_base, kTmemCols);
+}
+
+}  // namespace grp
+
+bool grouped_prefill_supported(const PrefillArgs& a, bool e4m3)
+{
+    return !e4m3 && a.G >= 1 && a.G <= grp::kM &&
+           (int64_t)a.kv_len <= (int64_t)4 * 32 * kGroupMaxWords;
+}
+
+int grouped_prefill_rows(const PrefillArgs& a, int sms, int rows_per_group)
+{
+    const int rg_max = grp::kM / a.G;
+    if (rows_per_group > 0)
+        return min(rows_per_group, rg_max);
+    // Fill whole waves of one CTA per SM with units as large as that allows.
+    const int64_t units_min = (int64_t)((a.R + rg_max - 1) / rg_max) * a.Hkv;
+    const int64_t waves = (units_min + sms - 1) / sms;
+    const int64_t groups = std::max<int64_t>(1, waves * sms / a.Hkv);
+    return (int)std::min<int64_t>(rg_max, (a.R + groups - 1) / groups);
+}
+
+cudaError_t launch_prefill_grouped(const PrefillArgs& a, int rows_per_group, cudaStream_t s)
+{
+    static std::atomic<int> attr_done[kMaxDevices];
+    static std::atomic<int> sm_count[kMaxDevices];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 0 || dev >= kMaxDevices)
+        return cudaErrorInvalidDevice;
+    int sms = sm_count[dev].load(std::memory_order_acquire);
+    if (sms == 0) {
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess)
+            return e;
+        sm_count[dev].store(sms, std::memory_order_release);
+    }
+    if (!attr_done[dev].load(std::memory_order_acquire)) {
+        e = cudaFuncSetAttribute(grp::sparse_prefill_grouped_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)grp::kSmemBytes);
+        if (e != cudaSuccess)
+            return e;
+        attr_done[dev].store(1, std::memory_order_release);
+    }
+    GroupArgs ga{};
+    ga.a = a;
+    ga.Rg = grouped_prefill_rows(a, sms, rows_per_group);
+    const int64_t groups = (a.R + ga.Rg - 1) / ga.Rg;
+    ga.n_units = (int)(groups * a.Hkv);
+    const int64_t blocks = a.kv_len > 0 ? ((int64_t)a.kv_len + 3) / 4 : 1;
+    ga.nbw = (int)std::max<int64_t>(1, (blocks + 31) / 32);
+    const int grid = std::min(ga.n_units, sms);
+    grp::sparse_prefill_grouped_kernel<<<grid, grp::kThreads, grp::kSmemBytes, s>>>(ga);
+    return cudaGetLastError();
+}
+
+}  // namespace pgqa

@@ -74,6 +74,7 @@ typedef enum {
 #define PAGED_GQA_FLAG_BAD_SEL     16  /* selected block at or after the row's own block: skipped   */
 #define PAGED_GQA_FLAG_SCORES_SHORT 32  /* a selection row has more causal blocks than scores given  */
 #define PAGED_GQA_FLAG_BAD_LOGIT   64  /* a masking row's largest logit is NaN or +inf: top-p skipped */
+#define PAGED_GQA_FLAG_TIMEOUT    128  /* a kernel's bounded wait ran out (never expected); output invalid */
 
 typedef enum {
     PAGED_GQA_KV_FP16 = 0,            /* binary16 K/V                            */
@@ -199,7 +200,8 @@ int paged_gqa_decode_noalloc(const void* q, const void* k_cache, const void* v_c
  *               (PAGED_GQA_FLAG_QPOS_CLAMPED).
  *  page_size    a multiple of 4, so a four-token block never straddles pages.
  *  out          device, binary16 [R, Hq, D] contiguous; fully written.
- * One kernel is launched; no workspace is needed.
+ * One kernel is launched; no workspace is needed.  This entry point takes
+ * the per-row route of paged_gqa_sparse_prefill_route below.
  */
 int paged_gqa_sparse_prefill(const void* q, const void* k_cache, const void* v_cache,
                              paged_gqa_kv_layout kv_layout, int kv_dtype,
@@ -208,6 +210,38 @@ int paged_gqa_sparse_prefill(const void* q, const void* k_cache, const void* v_c
                              int R, int Hq, int Hkv, int D, int page_size,
                              float kv_scale, float softmax_scale,
                              void* out, int* err_flag, void* stream);
+
+/*
+ * paged_gqa_sparse_prefill with the kernel route chosen by the caller (for
+ * testing and comparing the two designs; results agree within rounding):
+ *  route = PAGED_GQA_PREFILL_AUTO     the choice paged_gqa_sparse_prefill makes
+ *                                     (currently the per-row route);
+ *          PAGED_GQA_PREFILL_ROWWISE  one CTA per (row, KV head): each row's
+ *                                     blocks are gathered for that row alone;
+ *          PAGED_GQA_PREFILL_GROUPED  one CTA per group of consecutive rows
+ *                                     of one KV head (128 query-head slots at
+ *                                     most): the union of the group's blocks
+ *                                     is gathered once into shared memory and
+ *                                     each row masks the tokens it attends;
+ *                                     tcgen05 tensor cores, TMEM accumulators.
+ *                                     FP16 caches and kv_len <= 131072 only
+ *                                     (else PAGED_GQA_ERR_UNSUPPORTED).
+ *  rows_per_group  grouped route: rows of one group, 1 .. 128 / (Hq / Hkv);
+ *                  0 = sized to fill whole waves of one CTA per SM.
+ * A listed block counts once per listing on both routes (duplicates are a
+ * caller error; the grouped route recounts such rows on a slow path).
+ */
+#define PAGED_GQA_PREFILL_AUTO     0
+#define PAGED_GQA_PREFILL_ROWWISE  1
+#define PAGED_GQA_PREFILL_GROUPED  2
+int paged_gqa_sparse_prefill_route(const void* q, const void* k_cache, const void* v_cache,
+                                   paged_gqa_kv_layout kv_layout, int kv_dtype,
+                                   const int32_t* block_table, int num_pages, int kv_len,
+                                   const int32_t* sel_idx, int n_sel, const int32_t* q_pos,
+                                   int R, int Hq, int Hkv, int D, int page_size,
+                                   float kv_scale, float softmax_scale,
+                                   void* out, int* err_flag, void* stream,
+                                   int route, int rows_per_group);
 
 /*
  * QSA block selection ("[Kernel][SM70] Accelerate exact Qwen3.8 decode",

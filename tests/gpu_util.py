@@ -63,11 +63,15 @@ def run_prefill(case, kv=None, **kw):
         kv = dev_kv(case)
     _, k, v = kv
     err = t.zeros(1, dtype=t.int32, device="cuda")
-    out = P.paged_gqa_sparse_prefill(dev(case.q), k, v, dev(case.block_table), case.kv_len,
-                                     dev(case.sel_idx), dev(kw.pop("q_pos", case.q_pos)),
-                                     case.page_size, case.softmax_scale, case.kv_scale,
-                                     num_pages=kw.pop("num_pages", case.num_pages), err_flag=err,
-                                     **kw)
+    route, rows = kw.pop("route", None), kw.pop("rows_per_group", 0)
+    args = (dev(case.q), k, v, dev(case.block_table), case.kv_len, dev(case.sel_idx),
+            dev(kw.pop("q_pos", case.q_pos)), case.page_size, case.softmax_scale, case.kv_scale)
+    num_pages = kw.pop("num_pages", case.num_pages)
+    if route is None:
+        out = P.paged_gqa_sparse_prefill(*args, num_pages=num_pages, err_flag=err, **kw)
+    else:
+        out = P.paged_gqa_sparse_prefill_route(*args, route=route, rows_per_group=rows,
+                                               num_pages=num_pages, err_flag=err, **kw)
     t.cuda.synchronize()
     return out.cpu().numpy(), int(err.item())
 

@@ -57,13 +57,14 @@ def test_flag_bits_match_header_and_oracle():
     bits = {m.group(1): int(m.group(2))
             for m in re.finditer(r"#define PAGED_GQA_FLAG_(\w+)\s+(\d+)", text)}
     assert bits == {"BAD_PAGE": 1, "SEQ_CLAMPED": 2, "EMPTY_ROW": 4, "QPOS_CLAMPED": 8,
-                    "BAD_SEL": 16, "SCORES_SHORT": 32, "BAD_LOGIT": 64}
+                    "BAD_SEL": 16, "SCORES_SHORT": 32, "BAD_LOGIT": 64, "TIMEOUT": 128}
     assert (oracle.FLAG_BAD_PAGE, oracle.FLAG_SEQ_CLAMPED, oracle.FLAG_EMPTY_ROW,
             oracle.FLAG_QPOS_CLAMPED, oracle.FLAG_BAD_SEL) == (1, 2, 4, 8, 16)
     assert (P.FLAG_BAD_PAGE, P.FLAG_SEQ_CLAMPED, P.FLAG_EMPTY_ROW, P.FLAG_QPOS_CLAMPED,
             P.FLAG_BAD_SEL) == (1, 2, 4, 8, 16)
     assert oracle.FLAG_SCORES_SHORT == P.FLAG_SCORES_SHORT == 32
     assert P.FLAG_BAD_LOGIT == 64
+    assert P.FLAG_TIMEOUT == 128
 
 
 A = 0x10000   # a fake, 16-byte aligned, non-NULL address (never dereferenced)
@@ -148,6 +149,30 @@ def _prefill(L, **kw):
 @host_only
 def test_prefill_rejects_bad_arguments(L, kw, status):
     assert _prefill(L, **kw) == status
+
+
+def _prefill_route(L, route, rows, **kw):
+    args = dict(q=A, k=A, v=A, layout=(16 * 512, 512, 256), dtype=0, bt=A, num_pages=2048,
+                kv_len=32768, sel=A, n_sel=512, qp=A, R=4096, Hq=6, Hkv=1, D=256, P=16,
+                kv_scale=1.0, s=0.0625, out=A, err=None)
+    args.update(kw)
+    return L.paged_gqa_sparse_prefill_route(
+        args["q"], args["k"], args["v"], P.KVLayout(*args["layout"]), args["dtype"], args["bt"],
+        args["num_pages"], args["kv_len"], args["sel"], args["n_sel"], args["qp"], args["R"],
+        args["Hq"], args["Hkv"], args["D"], args["P"], args["kv_scale"], args["s"], args["out"],
+        args["err"], None, route, rows)
+
+
+@pytest.mark.parametrize("route,rows,kw,status", [
+    (3, 0, {}, -3), (-1, 0, {}, -3), (2, -1, {}, -3),
+    (2, 22, {}, -3),                               # 22 rows x 6 heads > 128 slots
+    (2, 0, dict(dtype=1), -4),                     # grouped route: FP16 caches only
+    (2, 0, dict(kv_len=131076, num_pages=8193), -4),   # beyond the union bitmap
+    (1, 0, dict(q=None), -1), (2, 0, dict(D=64), -4),
+])
+@host_only
+def test_prefill_route_rejects_bad_arguments(L, route, rows, kw, status):
+    assert _prefill_route(L, route, rows, **kw) == status
 
 
 @host_only

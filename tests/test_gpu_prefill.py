@@ -14,8 +14,15 @@ def _built():
     __graft_entry__.build()
 
 
-def _check_full(case, **kw):
-    got, flags = U.run_prefill(case, **kw)
+# Kernel routes: the per-row kernel, and the grouped tcgen05 kernel with the
+# automatic group size and with forced sizes (the largest group of 128 slots,
+# and a small one that leaves a ragged last group).
+ROUTES = [dict(route=1), dict(route=2), dict(route=2, rows_per_group=3)]
+ROUTE_IDS = ["rowwise", "grouped", "grouped3"]
+
+
+def _check_full(case, route=None, **kw):
+    got, flags = U.run_prefill(case, **(route or {}))
     want, _, oflags = U.oracle_prefill(case, **kw)
     U.assert_close(got, want, case.name)
     assert flags == oflags, f"{case.name}: flags {flags} != oracle {oflags}"
@@ -34,27 +41,76 @@ def test_small_layouts_and_dtypes(kvd, interleaved):
     _check_full(_small(100, kv_dtype=kvd, interleaved=interleaved))
 
 
+@pytest.mark.parametrize("interleaved", [True, False])
+@pytest.mark.parametrize("route", ROUTES, ids=ROUTE_IDS)
+def test_small_layouts_fp16_routes(route, interleaved):
+    _check_full(_small(101, interleaved=interleaved), route)
+
+
+@pytest.mark.parametrize("route", ROUTES, ids=ROUTE_IDS)
 @pytest.mark.parametrize("tail", [1, 2, 3, 4])
-def test_each_tail_length(tail):
-    _check_full(_small(110 + tail, tails=(tail,)))
+def test_each_tail_length(tail, route):
+    _check_full(_small(110 + tail, tails=(tail,)), route)
 
 
+@pytest.mark.parametrize("route", ROUTES, ids=ROUTE_IDS)
 @pytest.mark.parametrize("n_sel", [0, 1, 2, 3, 5, 511, 512])
-def test_selection_counts(n_sel):
-    _check_full(_small(120, n_sel=n_sel, first_block=max(n_sel, 8), R=9))
+def test_selection_counts(n_sel, route):
+    _check_full(_small(120, n_sel=n_sel, first_block=max(n_sel, 8), R=9), route)
 
 
+@pytest.mark.parametrize("route", ROUTES, ids=ROUTE_IDS)
 @pytest.mark.parametrize("page_size", [4, 8, 48, 784])
-def test_page_sizes(page_size):
-    _check_full(_small(130, page_size=page_size))
+def test_page_sizes(page_size, route):
+    _check_full(_small(130, page_size=page_size), route)
 
 
-def test_grouped_heads_and_single_row():
-    _check_full(_small(140, Hq=12, Hkv=2))
-    _check_full(_small(141, Hq=16, Hkv=2, R=1))
+@pytest.mark.parametrize("route", ROUTES, ids=ROUTE_IDS)
+def test_grouped_heads_and_single_row(route):
+    _check_full(_small(140, Hq=12, Hkv=2), route)
+    _check_full(_small(141, Hq=16, Hkv=2, R=1), route)
 
 
-def test_unsorted_selection_and_inert_entries():
+@pytest.mark.parametrize("rows", [1, 2, 5, 16, 21])
+def test_grouped_route_group_sizes(rows):
+    """Groups of 1 .. 21 rows (126 of 128 slots at six heads per KV head),
+    37 rows so most sizes leave a ragged last group."""
+    _check_full(_small(160, R=37, n_sel=48, first_block=64), dict(route=2, rows_per_group=rows))
+
+
+@pytest.mark.parametrize("route", ROUTES, ids=ROUTE_IDS)
+def test_peaked_scores_rescale(route):
+    """softmax_scale 1 makes scores spread over ~+-50 in the log2 domain, so
+    the running maxima keep rising by more than the rescale slack of the
+    grouped kernel and O is rescaled in tensor memory many times."""
+    c = _small(170, R=21, n_sel=64, first_block=96)
+    c.softmax_scale = 1.0
+    _check_full(c, route)
+
+
+@pytest.mark.parametrize("route", ROUTES, ids=ROUTE_IDS)
+def test_duplicated_selections_count_per_listing(route):
+    """A caller error that still has a meaning: a block listed twice counts
+    twice (the oracle attends its tokens twice); the grouped kernel takes its
+    slow recount path for such rows."""
+    c = _small(180, R=21, n_sel=40, first_block=64)
+    c.sel_idx[2, 1] = c.sel_idx[2, 0]
+    c.sel_idx[5, 3] = c.sel_idx[5, 7] = c.sel_idx[5, 9]
+    c.sel_idx[9, :] = c.sel_idx[9, 0]
+    _check_full(c, route)
+
+
+def test_grouped_route_union_in_two_mask_windows():
+    """21 rows of 2048 selections each over ~8000 earlier blocks: the union
+    (~8000 blocks, ~500 stages) exceeds the mask capacity of a 21-row group
+    (390 stages), so the stage masks are rebuilt for a second window."""
+    c = _small(190, R=21, n_sel=2048, first_block=8000, tails=(1, 2, 3))
+    _check_full(c, dict(route=2, rows_per_group=21))
+    _check_full(c, dict(route=1))
+
+
+@pytest.mark.parametrize("route", ROUTES, ids=ROUTE_IDS)
+def test_unsorted_selection_and_inert_entries(route):
     c = _small(150)
     rng = np.random.default_rng(5)
     for r in range(c.R):
@@ -65,8 +121,18 @@ def test_unsorted_selection_and_inert_entries():
     c.q_pos[6] = -2                            # zero row, flagged
     c.q_pos[7] = c.kv_len + 100                # clamped, flagged
     c.block_table[2] = -1                      # a hole in the page table
-    got = _check_full(c)
+    got = _check_full(c, route)
     assert np.all(got[6] == 0)
+
+
+def test_routes_agree_at_4096_rows_and_grouped_is_deterministic():
+    c = W.sparse_prefill_4096()
+    grouped, f1 = U.run_prefill(c, route=2)
+    rowwise, f2 = U.run_prefill(c, route=1)
+    assert f1 == 0 and f2 == 0
+    U.assert_close(grouped, rowwise.astype(np.float64), c.name + " grouped vs rowwise")
+    again, _ = U.run_prefill(c, route=2)
+    assert np.array_equal(grouped.view(np.uint16), again.view(np.uint16)), "run-to-run"
 
 
 def test_full_4096_rows_sampled():
