@@ -17,7 +17,9 @@ step (~470 MB) exceed L2 as well.
 The same line reports the selected-sparse prefill (4096 rows, 512 selected
 four-token blocks + a 1..3-token tail, Hq6/Hkv1/D256 FP16, interleaved K/V,
 32768-token cache) timed the same way, the same prefill over an E4M3 copy of
-the cache, the QSA block selection that produces such selections (4096 rows
+the cache, the same FP16 rows on the grouped tcgen05 route (union of each row
+group's blocks gathered once; its gathered bytes and tensor-core rate), both
+prefill routes on denser selections (2048 blocks per row), the QSA block selection that produces such selections (4096 rows
 of 8192 block scores, k = 512), the decode step's top-k/top-p masking of
 16 x 248,320 logits (k = 20, p = 0.95), the roofline of the dominant kernel
 (the decode split kernel, timed by CUDA events the library records around it
@@ -48,6 +50,7 @@ sys.path.insert(0, ROOT)
 
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 
 
 # ------------------------------------------------------------------ bookkeeping
@@ -66,6 +69,32 @@ def prefill_tokens(case) -> int:
     sel = (case.sel_idx >= 0) & (case.sel_idx < own[:, None])
     live = case.q_pos >= 0
     return int(4 * sel[live].sum() + (p - 4 * own + 1)[live].sum())
+
+
+def grouped_union(case, rows_per_group):
+    """(union blocks, 64-token stages) of the grouped route over the case's
+    row groups: per group, the distinct attended blocks (selected blocks
+    before each row's own block, plus the own blocks)."""
+    p = np.minimum(case.q_pos.astype(np.int64), case.kv_len - 1)
+    own = p // 4
+    total = stages = 0
+    for r0 in range(0, case.R, rows_per_group):
+        r1 = min(case.R, r0 + rows_per_group)
+        live = case.q_pos[r0:r1] >= 0
+        sel = case.sel_idx[r0:r1].astype(np.int64)
+        ok = (sel >= 0) & (sel < own[r0:r1, None]) & live[:, None]
+        n = len(np.unique(np.concatenate([sel[ok], own[r0:r1][live]])))
+        total += n
+        stages += -(-n // 16)
+    return total, stages
+
+
+def measured_bf16_tflops():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"])
+    return FALLBACK_BF16_TFLOPS
 
 
 def source_hash() -> str:
@@ -356,8 +385,8 @@ def run_ours(args, rank, world):
         return sum(a_ev[i].elapsed_time(b_ev[i]) for i in range(Kp)) / Kp
 
     # ---- selected-sparse prefill, 4096 rows, FP16 and E4M3 caches
-    def prefill_phase(kv_dtype):
-        pc = W.sparse_prefill_4096(kv_dtype=kv_dtype)
+    def prefill_phase(kv_dtype, route=P.PREFILL_AUTO, pc=None):
+        pc = pc if pc is not None else W.sparse_prefill_4096(kv_dtype=kv_dtype)
         pkv = torch.from_numpy(pc.kv).to(dev)
         pk, pv = pkv[:, :, :, 0, :], pkv[:, :, :, 1, :]
         pq = torch.from_numpy(pc.q).to(dev)
@@ -365,9 +394,9 @@ def run_ours(args, rank, world):
         psel = torch.from_numpy(pc.sel_idx).to(dev)
         ppos = torch.from_numpy(pc.q_pos).to(dev)
         pout = torch.empty_like(pq)
-        ms = time_phase(lambda: P.paged_gqa_sparse_prefill(
+        ms = time_phase(lambda: P.paged_gqa_sparse_prefill_route(
             pq, pk, pv, pbt, pc.kv_len, psel, ppos, pc.page_size, pc.softmax_scale,
-            pc.kv_scale, pout))
+            pc.kv_scale, pout, route=route))
         toks = prefill_tokens(pc)
         gathered = toks * pc.Hkv * 2 * pc.D * pc.kv.itemsize
         flops = 4.0 * toks * pc.Hq * pc.D      # QK^T and PV, 2 flops per multiply-add
@@ -375,6 +404,19 @@ def run_ours(args, rank, world):
 
     pc, p_ms, toks, gathered, flops = prefill_phase("fp16")
     pc8, p8_ms, toks8, gathered8, _ = prefill_phase("e4m3")
+    # the same FP16 rows on the grouped tcgen05 route: the union of each row
+    # group's blocks is gathered once
+    _, g_ms, _, _, _ = prefill_phase("fp16", route=P.PREFILL_GROUPED, pc=pc)
+    g_rows = P.paged_gqa_sparse_prefill_group_rows(pc.R, pc.Hq, pc.Hkv)
+    g_blocks, g_tiles = grouped_union(pc, g_rows)
+    g_bytes = g_blocks * 4 * pc.Hkv * 2 * pc.D * pc.kv.itemsize
+    g_mma = g_tiles * pc.Hkv * 2.0 * (2 * 128 * 64 * 256)   # Q K^T and P V per 64-token stage
+    # denser selections (2048 blocks per row): where the grouped route wins
+    pcd = W.prefill_case("sparse_prefill_r4096_sel2048", R=4096, n_sel=2048, seed=5,
+                         first_block=4096, kv_len=32768)
+    _, d_row_ms, _, _, _ = prefill_phase("fp16", route=P.PREFILL_ROWWISE, pc=pcd)
+    _, d_grp_ms, _, _, _ = prefill_phase("fp16", route=P.PREFILL_GROUPED, pc=pcd)
+    del pcd
 
     # ---- QSA block selection: 4096 rows of 8192 block scores, k = 512
     sc = W.qsa_select_4096()
@@ -446,6 +488,23 @@ def run_ours(args, rank, world):
             "gathered_GBps": round(gathered / (p_ms * 1e-3) / 1e9, 1),
             "tflops": round(flops / (p_ms * 1e-3) / 1e12, 2),
             "pages_context_ms_v100": 8.84736,
+        },
+        "sparse_prefill_grouped": {
+            "workload": "the FP16 4096-row workload above on the grouped tcgen05 route "
+                        "(paged_gqa_sparse_prefill_route, PREFILL_GROUPED)",
+            "ms": round(g_ms, 4), "rows_per_group": g_rows, "union_blocks": g_blocks,
+            "gathered_bytes": g_bytes, "gathered_vs_rowwise": round(g_bytes / gathered, 4),
+            "gathered_GBps": round(g_bytes / (g_ms * 1e-3) / 1e9, 1),
+            "mma_tflops": round(g_mma / (g_ms * 1e-3) / 1e12, 1),
+            "tensor_frac": round(g_mma / (g_ms * 1e-3) / 1e12 / measured_bf16_tflops(), 4),
+            "tensor_peak": "measured bf16_tflops (kind::f16 runs at the bf16 rate)",
+            "useful_tflops": round(flops / (g_ms * 1e-3) / 1e12, 2),
+        },
+        "sparse_prefill_dense": {
+            "workload": "4096 rows, 2048 selected four-token blocks per row (a quarter to a "
+                        "half of the candidates), otherwise as above",
+            "rowwise_ms": round(d_row_ms, 4), "grouped_ms": round(d_grp_ms, 4),
+            "auto_route": "grouped (32 n_sel >= kv_len)",
         },
         "sparse_prefill_e4m3": {
             "workload": "the same 4096 rows over an E4M3 copy of the cache (per-tensor scale)",

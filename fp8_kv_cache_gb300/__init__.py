@@ -27,7 +27,7 @@ __all__ = [
     "PagedGQAError", "library_path", "lib", "KV_FP16", "KV_E4M3",
     "FLAG_BAD_PAGE", "FLAG_SEQ_CLAMPED", "FLAG_EMPTY_ROW", "FLAG_QPOS_CLAMPED", "FLAG_BAD_SEL",
     "paged_gqa_decode", "paged_gqa_decode_noalloc", "paged_gqa_sparse_prefill",
-    "paged_gqa_sparse_prefill_route", "PREFILL_AUTO", "PREFILL_ROWWISE", "PREFILL_GROUPED",
+    "paged_gqa_sparse_prefill_route", "paged_gqa_sparse_prefill_group_rows", "PREFILL_AUTO", "PREFILL_ROWWISE", "PREFILL_GROUPED",
     "paged_gqa_gather_dequant",
     "paged_gqa_sparse_prefill_tokens", "paged_gqa_decode_workspace_size",
     "paged_gqa_decode_workspace_size_splits",
@@ -106,6 +106,8 @@ def lib():
                                                          vp, i32, vp, i32, i32, i32, i32, i32,
                                                          f32, f32, vp, vp, vp, i32, i32]
             L.paged_gqa_sparse_prefill_route.restype = i32
+            L.paged_gqa_sparse_prefill_group_rows.argtypes = [i32, i32, i32, i32]
+            L.paged_gqa_sparse_prefill_group_rows.restype = i32
             L.paged_gqa_gather_dequant.argtypes = [vp, KVLayout, i32, vp, i64, vp, i32, i32, i32,
                                                    i32, i32, i32, i32, f32, vp, vp]
             L.paged_gqa_gather_dequant.restype = i32
@@ -271,6 +273,13 @@ def paged_gqa_sparse_prefill_route(q, k_cache, v_cache, block_table, kv_len, sel
     _check(lib().paged_gqa_sparse_prefill_route(*args, int(route), int(rows_per_group)),
            "paged_gqa_sparse_prefill_route")
     return out
+
+
+def paged_gqa_sparse_prefill_group_rows(R, Hq, Hkv, rows_per_group=0) -> int:
+    """Rows per group of the grouped prefill route on the current device."""
+    n = lib().paged_gqa_sparse_prefill_group_rows(int(R), int(Hq), int(Hkv), int(rows_per_group))
+    _check(min(n, 0), "paged_gqa_sparse_prefill_group_rows")
+    return n
 
 
 def _prefill_args(q, k_cache, v_cache, block_table, kv_len, sel_idx, q_pos, page_size,

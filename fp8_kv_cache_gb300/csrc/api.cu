@@ -281,13 +281,39 @@ int paged_gqa_sparse_prefill_route(const void* q, const void* k_cache, const voi
         return PAGED_GQA_ERR_UNSUPPORTED;
     if (rows_per_group > kGroupSlots / a.G)
         return PAGED_GQA_ERR_SHAPE;
-    // The automatic choice is the per-row kernel: on the 4096-row workload it
-    // runs at the gather ceiling, ahead of the grouped kernel.
-    const bool grouped = route == PAGED_GQA_PREFILL_GROUPED;
+    // Automatic choice: the grouped kernel once rows select at least 1/8 of
+    // the sequence's blocks (32 n_sel >= kv_len), where the union of a row
+    // group is much smaller than the sum of its rows' selections; below that
+    // the per-row kernel, which gathers at the L2 ceiling, is faster (4096
+    // rows over 32768 tokens: crossover between 512 and 1024 selections).
+    const bool grouped = route == PAGED_GQA_PREFILL_GROUPED ||
+                         (route == PAGED_GQA_PREFILL_AUTO && grouped_ok &&
+                          (int64_t)32 * n_sel >= (int64_t)kv_len);
     const cudaError_t e =
         grouped ? launch_prefill_grouped(a, rows_per_group, static_cast<cudaStream_t>(stream))
                 : launch_prefill(a, e4m3, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PAGED_GQA_OK : PAGED_GQA_ERR_CUDA;
+}
+
+int paged_gqa_sparse_prefill_group_rows(int R, int Hq, int Hkv, int rows_per_group)
+{
+    if (R < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || rows_per_group < 0)
+        return PAGED_GQA_ERR_SHAPE;
+    if (Hq / Hkv > kGMax)
+        return PAGED_GQA_ERR_UNSUPPORTED;
+    if (rows_per_group > kGroupSlots / (Hq / Hkv))
+        return PAGED_GQA_ERR_SHAPE;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        sms <= 0)
+        return PAGED_GQA_ERR_CUDA;
+    PrefillArgs a{};
+    a.R = R;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.G = Hq / Hkv;
+    return grouped_prefill_rows(a, sms, rows_per_group);
 }
 
 int paged_gqa_gather_dequant(const void* cache, paged_gqa_kv_layout kv_layout, int kv_dtype,

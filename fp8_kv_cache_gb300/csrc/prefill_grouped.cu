@@ -379,24 +379,27 @@ __device__ void issue_mma(Smem& sm, Cursor& cur, int nt)
             if (g >= 2)
                 wait_or_abort(sm, &sm.s_free[buf], ((g >> 1) - 1) & 1);
             tc::fence_after_sync();
+            // descriptors advance by their 16-byte address field: K steps of
+            // 16 elements are 32 bytes inside a row, every 4th a new region
+            const uint64_t db0 = tc::sw128_desc(st, 16, 1024);
+            const uint32_t d = tm + kTmemS + 64 * buf;
 #pragma unroll
-            for (int kk = 0; kk < kD / 16; ++kk) {
-                const uint32_t off = (kk & 3) * 32;
-                const uint64_t db = tc::sw128_desc(st + (kk >> 2) * kRegionBytes + off, 16, 1024);
-                tc::mma_ts(tm + kTmemS + 64 * buf, tm + kTmemQ + 8 * kk, db, kIdQK, kk > 0);
-            }
+            for (int kk = 0; kk < kD / 16; ++kk)
+                tc::mma_ts(d, tm + kTmemQ + 8 * kk,
+                           db0 + (uint64_t)(((kk >> 2) * kRegionBytes + (kk & 3) * 32) >> 4), kIdQK,
+                           kk > 0);
             tc::mma_commit(&sm.empty[s]);
             tc::mma_commit(&sm.s_full[buf]);
         } else {
             wait_or_abort(sm, &sm.p_full[buf], (g >> 1) & 1);
             tc::fence_after_sync();
-            const uint32_t pa = tc::smem_addr(sm.p[buf]);
+            const uint64_t da0 = tc::sw128_desc(tc::smem_addr(sm.p[buf]), 16, 1024);
+            const uint64_t db0 = tc::sw128_desc(st, kRegionBytes, 1024);
+            const uint32_t acc0 = ht > 0;
 #pragma unroll
-            for (int kk = 0; kk < kStageTokens / 16; ++kk) {
-                const uint64_t da = tc::sw128_desc(pa + kk * 32, 16, 1024);
-                const uint64_t db = tc::sw128_desc(st + kk * 2048, kRegionBytes, 1024);
-                tc::mma_ss(tm + kTmemO, da, db, kIdPV, (ht > 0 || kk > 0));
-            }
+            for (int kk = 0; kk < kStageTokens / 16; ++kk)
+                tc::mma_ss(tm + kTmemO, da0 + (uint64_t)(kk * 2), db0 + (uint64_t)(kk * 128), kIdPV,
+                           kk > 0 ? 1u : acc0);
             tc::mma_commit(&sm.empty[s]);
             tc::mma_commit(&sm.p_free[buf]);
         }
@@ -453,11 +456,13 @@ __device__ void softmax_unit(const GroupArgs& ga, Smem& sm, Cursor& cur, int r0,
         uint32_t live = 0u;
         if (own >= 0) {
             const int li = i - ht0;
-            const uint32_t m8 =
+            uint32_t x8 =
                 (sm.masks[rl * words_per_row + (li >> 1)] >> (((li & 1) << 4) + 8 * half)) & 0xFFu;
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-                live |= ((m8 >> k) & 1u) ? (0xFu << (4 * k)) : 0u;
+            // spread bit k to bit 4k, then fill each nibble
+            x8 = (x8 | (x8 << 12)) & 0x000F000Fu;
+            x8 = (x8 | (x8 << 6)) & 0x03030303u;
+            x8 = (x8 | (x8 << 3)) & 0x11111111u;
+            live = x8 * 0xFu;
             if (rank_own >= 0 && (rank_own >> 4) == i) {
                 const int ko = (rank_own & 15) - 8 * half;
                 if (ko >= 0 && ko < 8)

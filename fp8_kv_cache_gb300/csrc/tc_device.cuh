@@ -25,7 +25,8 @@
 namespace pgqa {
 namespace tc {
 
-constexpr long kSpinLimit = 1L << 26;   // try_wait polls before a wait gives up
+constexpr long kSpinLimit = 1L << 20;   // try_wait polls before a wait gives up
+constexpr uint32_t kSuspendNs = 2000;   // a poll may sleep this long unless the phase completes
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p)
 {
@@ -51,17 +52,19 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar)
 }
 
 // Waits until the phase of parity `par` of *bar has completed; false when the
-// poll limit ran out first.
+// poll limit ran out first (about two seconds at most).  Each poll may
+// suspend the thread until the phase completes, so waiting warps leave their
+// issue slots to the warps that work.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t par)
 {
     const uint32_t a = smem_addr(bar);
     for (long it = 0; it < kSpinLimit; ++it) {
         uint32_t ok;
         asm volatile("{\n\t.reg .pred p;\n\t"
-                     "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                     "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
                      "selp.u32 %0, 1, 0, p;\n\t}"
                      : "=r"(ok)
-                     : "r"(a), "r"(par)
+                     : "r"(a), "r"(par), "r"(kSuspendNs)
                      : "memory");
         if (ok)
             return true;

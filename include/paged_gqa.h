@@ -200,8 +200,8 @@ int paged_gqa_decode_noalloc(const void* q, const void* k_cache, const void* v_c
  *               (PAGED_GQA_FLAG_QPOS_CLAMPED).
  *  page_size    a multiple of 4, so a four-token block never straddles pages.
  *  out          device, binary16 [R, Hq, D] contiguous; fully written.
- * One kernel is launched; no workspace is needed.  This entry point takes
- * the per-row route of paged_gqa_sparse_prefill_route below.
+ * One kernel is launched; no workspace is needed.  The kernel route is the
+ * automatic one of paged_gqa_sparse_prefill_route below.
  */
 int paged_gqa_sparse_prefill(const void* q, const void* k_cache, const void* v_cache,
                              paged_gqa_kv_layout kv_layout, int kv_dtype,
@@ -214,8 +214,10 @@ int paged_gqa_sparse_prefill(const void* q, const void* k_cache, const void* v_c
 /*
  * paged_gqa_sparse_prefill with the kernel route chosen by the caller (for
  * testing and comparing the two designs; results agree within rounding):
- *  route = PAGED_GQA_PREFILL_AUTO     the choice paged_gqa_sparse_prefill makes
- *                                     (currently the per-row route);
+ *  route = PAGED_GQA_PREFILL_AUTO     grouped for FP16 caches with kv_len <=
+ *                                     131072 when 32 * n_sel >= kv_len (dense
+ *                                     selections: the row groups' unions are
+ *                                     small), per-row otherwise;
  *          PAGED_GQA_PREFILL_ROWWISE  one CTA per (row, KV head): each row's
  *                                     blocks are gathered for that row alone;
  *          PAGED_GQA_PREFILL_GROUPED  one CTA per group of consecutive rows
@@ -231,6 +233,17 @@ int paged_gqa_sparse_prefill(const void* q, const void* k_cache, const void* v_c
  * A listed block counts once per listing on both routes (duplicates are a
  * caller error; the grouped route recounts such rows on a slow path).
  */
+/*
+ * Rows per group of the grouped route for R query rows of Hq / Hkv heads on
+ * the current device, given rows_per_group as passed to
+ * paged_gqa_sparse_prefill_route (0 = automatic: groups sized so the units
+ * fill whole waves of one CTA per SM).  Returns the count, or a negative
+ * status: PAGED_GQA_ERR_SHAPE (R < 1, Hq % Hkv != 0, rows_per_group out of
+ * range), PAGED_GQA_ERR_UNSUPPORTED (more than 8 query heads per KV head),
+ * PAGED_GQA_ERR_CUDA (no device to query).  Host only; launches nothing.
+ */
+int paged_gqa_sparse_prefill_group_rows(int R, int Hq, int Hkv, int rows_per_group);
+
 #define PAGED_GQA_PREFILL_AUTO     0
 #define PAGED_GQA_PREFILL_ROWWISE  1
 #define PAGED_GQA_PREFILL_GROUPED  2

@@ -175,6 +175,14 @@ def test_prefill_route_rejects_bad_arguments(L, route, rows, kw, status):
     assert _prefill_route(L, route, rows, **kw) == status
 
 
+@pytest.mark.parametrize("args,status", [
+    ((0, 6, 1, 0), -3), ((10, 7, 2, 0), -3), ((10, 6, 1, -1), -3), ((10, 6, 1, 22), -3),
+    ((10, 12, 1, 0), -4),
+])
+def test_group_rows_rejects_bad_arguments(L, args, status):
+    assert L.paged_gqa_sparse_prefill_group_rows(*args) == status
+
+
 @host_only
 def test_prefill_empty_cases_are_no_ops(L):
     assert _prefill(L, R=0) == 0
