@@ -97,11 +97,16 @@ def measured_bf16_tflops():
     return FALLBACK_BF16_TFLOPS
 
 
+# Sources the decode split kernel is compiled from; its ncu traffic figure is
+# tied to their hash.
+DECODE_SOURCES = ("decode.cu", "pgqa_device.cuh", "pgqa_internal.h")
+
+
 def source_hash() -> str:
-    """Hash of the CUDA sources; ncu traffic figures are tied to it."""
+    """Hash of the decode kernel's CUDA sources; ncu traffic figures are tied to it."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "fp8_kv_cache_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in DECODE_SOURCES:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -220,6 +225,8 @@ def run_ours(args, rank, world):
 
     if args.phase == "prefill":
         return run_prefill_only(args, dev)
+    if args.phase == "prefill-grouped":
+        return run_prefill_only(args, dev, route=2)
     if args.phase == "select":
         return run_select_only(args, dev)
     if args.phase == "mask":
@@ -534,8 +541,9 @@ def run_ours(args, rank, world):
     return line
 
 
-def run_prefill_only(args, dev):
-    """The sparse-prefill phase alone (for profiling)."""
+def run_prefill_only(args, dev, route=0):
+    """The sparse-prefill phase alone (for profiling); route as for
+    paged_gqa_sparse_prefill_route (0 = automatic, 2 = grouped)."""
     import torch
     import fp8_kv_cache_gb300 as P
     from fp8_kv_cache_gb300 import workloads as W
@@ -551,13 +559,13 @@ def run_prefill_only(args, dev):
     for i in range(args.warmup + args.steps):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
-        P.paged_gqa_sparse_prefill(pq, pk, pv, pbt, pc.kv_len, psel, ppos, pc.page_size,
-                                   pc.softmax_scale, pc.kv_scale, pout)
+        P.paged_gqa_sparse_prefill_route(pq, pk, pv, pbt, pc.kv_len, psel, ppos, pc.page_size,
+                                         pc.softmax_scale, pc.kv_scale, pout, route=route)
         b.record()
         torch.cuda.synchronize()
         if i >= args.warmup:
             ms.append(a.elapsed_time(b))
-    return {"phase": "prefill", "ms": float(np.mean(ms))}
+    return {"phase": "prefill" if route == 0 else "prefill-grouped", "ms": float(np.mean(ms))}
 
 
 def run_select_only(args, dev):
@@ -680,7 +688,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--phase", choices=["all", "decode", "prefill", "select", "mask"],
+    ap.add_argument("--phase", choices=["all", "decode", "prefill", "prefill-grouped", "select",
+                                        "mask"],
                     default="all",
                     help="run only one phase (for profiling); the JSON line needs 'all'")
     args = ap.parse_args()
