@@ -165,3 +165,36 @@ def test_full_4096_rows_contiguous_e4m3_sampled():
     rows = np.random.default_rng(8).choice(c.R, size=16, replace=False).astype(np.int32)
     want, _, _ = U.oracle_prefill(c, rows=rows)
     U.assert_close(got[rows], want[rows], c.name)
+
+
+@pytest.mark.parametrize("route", [1, 2], ids=["rowwise", "grouped"])
+def test_graph_replay_equals_eager(route):
+    """[P] Test Result: graph replay equal to eager.  The prefill captured in a
+    CUDA graph and replayed writes the same bits as the eager call, on the
+    hybrid 784-token pages of the same page ([P] Test Result: 784/16)."""
+    import torch
+    import fp8_kv_cache_gb300 as P
+    c = _small(200, R=40, n_sel=48, first_block=64, page_size=784)
+    _, k, v = U.dev_kv(c)
+    q, bt = U.dev(c.q), U.dev(c.block_table)
+    sel, pos = U.dev(c.sel_idx), U.dev(c.q_pos)
+
+    def call(out):
+        return P.paged_gqa_sparse_prefill_route(q, k, v, bt, c.kv_len, sel, pos, c.page_size,
+                                                c.softmax_scale, c.kv_scale, out,
+                                                route=route, num_pages=c.num_pages)
+
+    eager = call(torch.empty_like(q))
+    out = torch.empty_like(q)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        call(out)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            call(out)
+    out.fill_(7.0)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(eager.view(torch.int16), out.view(torch.int16))
+    want, _, _ = U.oracle_prefill(c)
+    U.assert_close(out.cpu().numpy(), want, c.name)
