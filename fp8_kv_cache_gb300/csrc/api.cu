@@ -281,16 +281,19 @@ int paged_gqa_sparse_prefill_route(const void* q, const void* k_cache, const voi
         return PAGED_GQA_ERR_UNSUPPORTED;
     if (rows_per_group > kGroupSlots / a.G)
         return PAGED_GQA_ERR_SHAPE;
-    // Automatic choice: the grouped kernel once rows select at least 1/8 of
-    // the sequence's blocks (32 n_sel >= kv_len), where the union of a row
-    // group is much smaller than the sum of its rows' selections; below that
-    // the per-row kernel, which gathers at the L2 ceiling, is faster (4096
-    // rows over 32768 tokens: crossover between 512 and 1024 selections).
+    // Automatic choice: the grouped kernel once rows select a large share of
+    // the sequence's blocks, where the union of a row group is much smaller
+    // than the sum of its rows' selections; below that the per-row kernel,
+    // which gathers at the L2 ceiling, is faster.  4096 rows over 32768
+    // tokens cross over between 512 and 1024 selections with FP16 rows
+    // (32 n_sel >= kv_len) and between 1024 and 2048 with E4M3 rows, whose
+    // per-row gather moves half the bytes (16 n_sel >= kv_len).
+    const int64_t density = e4m3 ? 16 : 32;
     const bool grouped = route == PAGED_GQA_PREFILL_GROUPED ||
                          (route == PAGED_GQA_PREFILL_AUTO && grouped_ok &&
-                          (int64_t)32 * n_sel >= (int64_t)kv_len);
+                          density * n_sel >= (int64_t)kv_len);
     const cudaError_t e =
-        grouped ? launch_prefill_grouped(a, rows_per_group, static_cast<cudaStream_t>(stream))
+        grouped ? launch_prefill_grouped(a, e4m3, rows_per_group, static_cast<cudaStream_t>(stream))
                 : launch_prefill(a, e4m3, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PAGED_GQA_OK : PAGED_GQA_ERR_CUDA;
 }

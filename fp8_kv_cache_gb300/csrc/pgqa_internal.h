@@ -97,7 +97,8 @@ cudaError_t launch_decode(const DecodeArgs& a, bool e4m3, cudaStream_t s, void* 
 cudaError_t launch_prefill(const PrefillArgs& a, bool e4m3, cudaStream_t s);
 bool grouped_prefill_supported(const PrefillArgs& a, bool e4m3);
 int grouped_prefill_rows(const PrefillArgs& a, int sms, int rows_per_group);
-cudaError_t launch_prefill_grouped(const PrefillArgs& a, int rows_per_group, cudaStream_t s);
+cudaError_t launch_prefill_grouped(const PrefillArgs& a, bool e4m3, int rows_per_group,
+                                   cudaStream_t s);
 cudaError_t launch_gather(const KVGeom& g, bool e4m3, const int32_t* bt, int64_t bt_stride,
                           const int32_t* seq_lens, int B, int T, int Hkv, int max_seq_len,
                           float kv_scale, float* out, cudaStream_t s);

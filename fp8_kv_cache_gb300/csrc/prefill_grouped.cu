@@ -1,5 +1,6 @@
 // prefill_grouped.cu -- selected-sparse paged prefill with grouped query rows
-// on the fifth-generation tensor cores (FP16 KV).
+// on the fifth-generation tensor cores (FP16 or E4M3 KV; the tensor cores see
+// binary16 tiles either way).
 //
 // Operation: "[Kernel][SM70] Accelerate Qwen3.8 QSA paged prefill"
 // (1Cat-vLLM #378), Changes: query row r with p = min(q_pos[r], kv_len - 1)
@@ -309,10 +310,14 @@ __device__ __forceinline__ void stage_of(int q, int nt, bool& is_v, int& ht)
 
 // Producer warps: warp pw owns ring slot pw and fills every stage that lands
 // there (stages it with it % kNS == pw): lanes 0..15 resolve the stage's 16
-// blocks (rank -> block -> page) in parallel, then each lane copies its
-// 16-byte chunk of all 64 rows.  The warp waits for its own copies, fences
-// them for the tensor cores and publishes the stage; stages of different
+// blocks (rank -> block -> page) in parallel.  FP16 rows: each lane copies its
+// 16-byte chunk of all 64 rows with cp.async and waits for its own copies.
+// E4M3 rows (256 codes): each lane loads 16-code chunks into registers,
+// converts them exactly to binary16 with the hardware converter and stores
+// the two 16-byte halves into the same tile layout.  The warp then fences its
+// writes for the tensor cores and publishes the stage; stages of different
 // warps are in flight together.
+template <bool kE4M3>
 __device__ void produce(const GroupArgs& ga, Smem& sm, Cursor& cur, int j, int nbw, int nt,
                         int n_union)
 {
@@ -338,23 +343,54 @@ __device__ void produce(const GroupArgs& ga, Smem& sm, Cursor& cur, int j, int n
             }
         }
         const unsigned char* base = is_v ? a.kv.v : a.kv.k;
-        const uint32_t st = tc::smem_addr(sm.ring[s]) + (lane >> 3) * kRegionBytes;
-        const uint32_t x = lane & 7;
-#pragma unroll 4
-        for (int blk = 0; blk < kStageBlocks; ++blk) {
-            const int64_t o = __shfl_sync(0xffffffffu, off, blk);
+        if (kE4M3) {
+            // chunk idx = lane + 32 i: row idx / 16, codes 16 (idx % 16) .. + 15
+            const uint32_t st = tc::smem_addr(sm.ring[s]);
+#pragma unroll 1
+            for (int part = 0; part < 4; ++part) {
+                uint4 raw[8];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int row = 4 * blk + u;
-                const uint32_t dst = st + row * 128 + ((x ^ (row & 7)) << 4);
-                const unsigned char* src = base + (o < 0 ? 0 : o + u * a.kv.token_b + 16 * lane);
-                asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-                             "r"(o < 0 ? 0 : 16)
-                             : "memory");
+                for (int i = 0; i < 8; ++i) {
+                    const int idx = lane + 32 * (8 * part + i), row = idx >> 4;
+                    const int64_t o = __shfl_sync(0xffffffffu, off, row >> 2);
+                    raw[i] = o < 0 ? make_uint4(0u, 0u, 0u, 0u)
+                                   : ldg_stream(base + o + (row & 3) * a.kv.token_b + 16 * (idx & 15));
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int idx = lane + 32 * (8 * part + i), row = idx >> 4, c16 = idx & 15;
+                    uint32_t h[8];
+                    e4m3x4_to_f16x2x2(raw[i].x, h[0], h[1]);
+                    e4m3x4_to_f16x2x2(raw[i].y, h[2], h[3]);
+                    e4m3x4_to_f16x2x2(raw[i].z, h[4], h[5]);
+                    e4m3x4_to_f16x2x2(raw[i].w, h[6], h[7]);
+                    const uint32_t rb = st + (c16 >> 2) * kRegionBytes + row * 128;
+                    const uint32_t x0 = 2 * (c16 & 3);
+                    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(rb + ((x0 ^ (row & 7)) << 4)),
+                                 "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3]) : "memory");
+                    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(rb + (((x0 + 1) ^ (row & 7)) << 4)),
+                                 "r"(h[4]), "r"(h[5]), "r"(h[6]), "r"(h[7]) : "memory");
+                }
             }
+        } else {
+            const uint32_t st = tc::smem_addr(sm.ring[s]) + (lane >> 3) * kRegionBytes;
+            const uint32_t x = lane & 7;
+#pragma unroll 4
+            for (int blk = 0; blk < kStageBlocks; ++blk) {
+                const int64_t o = __shfl_sync(0xffffffffu, off, blk);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int row = 4 * blk + u;
+                    const uint32_t dst = st + row * 128 + ((x ^ (row & 7)) << 4);
+                    const unsigned char* src = base + (o < 0 ? 0 : o + u * a.kv.token_b + 16 * lane);
+                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                                 "r"(o < 0 ? 0 : 16)
+                                 : "memory");
+                }
+            }
+            cp_async_commit();
+            cp_async_wait<0>();
         }
-        cp_async_commit();
-        cp_async_wait<0>();
         tc::fence_async_shared();
         tc::mbar_arrive(&sm.full[s]);
     }
@@ -579,7 +615,7 @@ __device__ void softmax_unit(const GroupArgs& ga, Smem& sm, Cursor& cur, int r0,
         wait_or_abort(sm, &sm.p_free[g_last & 1], (g_last >> 1) & 1);
         tc::fence_after_sync();
     }
-    const float inv = lt > 0.f ? 1.f / lt : 0.f;
+    const float inv = lt > 0.f ? a.v_scale / lt : 0.f;     // E4M3: the per-tensor scale of V
     uint4* dst = slot_ok ? reinterpret_cast<uint4*>(
                                a.out + ((size_t)(r0 + rl) * a.Hq + (size_t)j * a.G + h) * kD +
                                128 * half)
@@ -608,6 +644,7 @@ __device__ void softmax_unit(const GroupArgs& ga, Smem& sm, Cursor& cur, int r0,
     cur.g = g0 + nt;
 }
 
+template <bool kE4M3>
 __global__ void __launch_bounds__(kThreads, 1) sparse_prefill_grouped_kernel(const GroupArgs ga)
 {
     extern __shared__ unsigned char smem_raw[];
@@ -648,7 +685,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_prefill_grouped_kernel(con
         unit_setup(ga, sm, r0, Rg, j, ga.nbw, words_per_row, cap);
         const int nt = (sm.n_union + kStageBlocks - 1) / kStageBlocks;
         if (w >= kProdWarp0)
-            produce(ga, sm, cur, j, ga.nbw, nt, sm.n_union);
+            produce<kE4M3>(ga, sm, cur, j, ga.nbw, nt, sm.n_union);
         else if (w == kMmaWarp && lane == 0)
             issue_mma(sm, cur, nt);
         else if (w < kSoftWarps)
@@ -674,9 +711,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_prefill_grouped_kernel(con
 
 }  // namespace grp
 
-bool grouped_prefill_supported(const PrefillArgs& a, bool e4m3)
+bool grouped_prefill_supported(const PrefillArgs& a, bool)
 {
-    return !e4m3 && a.G >= 1 && a.G <= grp::kM &&
+    return a.G >= 1 && a.G <= grp::kM &&
            (int64_t)a.kv_len <= (int64_t)4 * 32 * kGroupMaxWords;
 }
 
@@ -692,9 +729,10 @@ int grouped_prefill_rows(const PrefillArgs& a, int sms, int rows_per_group)
     return (int)std::min<int64_t>(rg_max, (a.R + groups - 1) / groups);
 }
 
-cudaError_t launch_prefill_grouped(const PrefillArgs& a, int rows_per_group, cudaStream_t s)
+cudaError_t launch_prefill_grouped(const PrefillArgs& a, bool e4m3, int rows_per_group,
+                                   cudaStream_t s)
 {
-    static std::atomic<int> attr_done[kMaxDevices];
+    static std::atomic<int> attr_done[2][kMaxDevices];
     static std::atomic<int> sm_count[kMaxDevices];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -709,13 +747,16 @@ cudaError_t launch_prefill_grouped(const PrefillArgs& a, int rows_per_group, cud
             return e;
         sm_count[dev].store(sms, std::memory_order_release);
     }
-    if (!attr_done[dev].load(std::memory_order_acquire)) {
-        e = cudaFuncSetAttribute(grp::sparse_prefill_grouped_kernel,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)grp::kSmemBytes);
+    if (!attr_done[e4m3][dev].load(std::memory_order_acquire)) {
+        e = e4m3 ? cudaFuncSetAttribute(grp::sparse_prefill_grouped_kernel<true>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)grp::kSmemBytes)
+                 : cudaFuncSetAttribute(grp::sparse_prefill_grouped_kernel<false>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)grp::kSmemBytes);
         if (e != cudaSuccess)
             return e;
-        attr_done[dev].store(1, std::memory_order_release);
+        attr_done[e4m3][dev].store(1, std::memory_order_release);
     }
     GroupArgs ga{};
     ga.a = a;
@@ -725,7 +766,10 @@ cudaError_t launch_prefill_grouped(const PrefillArgs& a, int rows_per_group, cud
     const int64_t blocks = a.kv_len > 0 ? ((int64_t)a.kv_len + 3) / 4 : 1;
     ga.nbw = (int)std::max<int64_t>(1, (blocks + 31) / 32);
     const int grid = std::min(ga.n_units, sms);
-    grp::sparse_prefill_grouped_kernel<<<grid, grp::kThreads, grp::kSmemBytes, s>>>(ga);
+    if (e4m3)
+        grp::sparse_prefill_grouped_kernel<true><<<grid, grp::kThreads, grp::kSmemBytes, s>>>(ga);
+    else
+        grp::sparse_prefill_grouped_kernel<false><<<grid, grp::kThreads, grp::kSmemBytes, s>>>(ga);
     return cudaGetLastError();
 }
 

@@ -214,10 +214,11 @@ int paged_gqa_sparse_prefill(const void* q, const void* k_cache, const void* v_c
 /*
  * paged_gqa_sparse_prefill with the kernel route chosen by the caller (for
  * testing and comparing the two designs; results agree within rounding):
- *  route = PAGED_GQA_PREFILL_AUTO     grouped for FP16 caches with kv_len <=
- *                                     131072 when 32 * n_sel >= kv_len (dense
- *                                     selections: the row groups' unions are
- *                                     small), per-row otherwise;
+ *  route = PAGED_GQA_PREFILL_AUTO     grouped when kv_len <= 131072 and
+ *                                     32 * n_sel >= kv_len (FP16) or
+ *                                     16 * n_sel >= kv_len (E4M3): dense
+ *                                     selections, whose row-group unions are
+ *                                     small; per-row otherwise;
  *          PAGED_GQA_PREFILL_ROWWISE  one CTA per (row, KV head): each row's
  *                                     blocks are gathered for that row alone;
  *          PAGED_GQA_PREFILL_GROUPED  one CTA per group of consecutive rows
@@ -225,9 +226,10 @@ int paged_gqa_sparse_prefill(const void* q, const void* k_cache, const void* v_c
  *                                     most): the union of the group's blocks
  *                                     is gathered once into shared memory and
  *                                     each row masks the tokens it attends;
- *                                     tcgen05 tensor cores, TMEM accumulators.
- *                                     FP16 caches and kv_len <= 131072 only
- *                                     (else PAGED_GQA_ERR_UNSUPPORTED).
+ *                                     tcgen05 tensor cores, TMEM accumulators
+ *                                     (E4M3 rows are converted to binary16 as
+ *                                     they are gathered).  kv_len <= 131072
+ *                                     only (else PAGED_GQA_ERR_UNSUPPORTED).
  *  rows_per_group  grouped route: rows of one group, 1 .. 128 / (Hq / Hkv);
  *                  0 = sized to fill whole waves of one CTA per SM.
  * A listed block counts once per listing on both routes (duplicates are a

@@ -166,7 +166,6 @@ def _prefill_route(L, route, rows, **kw):
 @pytest.mark.parametrize("route,rows,kw,status", [
     (3, 0, {}, -3), (-1, 0, {}, -3), (2, -1, {}, -3),
     (2, 22, {}, -3),                               # 22 rows x 6 heads > 128 slots
-    (2, 0, dict(dtype=1), -4),                     # grouped route: FP16 caches only
     (2, 0, dict(kv_len=131076, num_pages=8193), -4),   # beyond the union bitmap
     (1, 0, dict(q=None), -1), (2, 0, dict(D=64), -4),
 ])

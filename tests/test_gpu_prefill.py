@@ -43,8 +43,19 @@ def test_small_layouts_and_dtypes(kvd, interleaved):
 
 @pytest.mark.parametrize("interleaved", [True, False])
 @pytest.mark.parametrize("route", ROUTES, ids=ROUTE_IDS)
-def test_small_layouts_fp16_routes(route, interleaved):
-    _check_full(_small(101, interleaved=interleaved), route)
+@pytest.mark.parametrize("kvd", ["fp16", "e4m3"])
+def test_small_layouts_routes(kvd, route, interleaved):
+    _check_full(_small(101, kv_dtype=kvd, interleaved=interleaved), route)
+
+
+@pytest.mark.parametrize("route", ROUTES, ids=ROUTE_IDS)
+def test_e4m3_inert_entries_and_tails(route):
+    c = _small(102, kv_dtype="e4m3", tails=(1, 2, 3, 4))
+    c.sel_idx[3, :5] = -1
+    c.sel_idx[4, 0] = c.q_pos[4] // 4
+    c.q_pos[6] = -2
+    c.block_table[1] = 10 ** 6
+    _check_full(c, route)
 
 
 @pytest.mark.parametrize("route", ROUTES, ids=ROUTE_IDS)
@@ -158,6 +169,16 @@ def test_full_4096_rows_interleaved_e4m3_sampled():
     assert flags == 0 and oflags == 0
 
 
+def test_full_4096_rows_e4m3_grouped_route_sampled():
+    c = W.sparse_prefill_4096(kv_dtype="e4m3")
+    got, flags = U.run_prefill(c, route=2)
+    rows = np.random.default_rng(11).choice(c.R, size=24, replace=False).astype(np.int32)
+    rows = np.concatenate([rows, [0, c.R - 1]]).astype(np.int32)
+    want, _, oflags = U.oracle_prefill(c, rows=rows)
+    U.assert_close(got[rows], want[rows], c.name + " grouped")
+    assert flags == 0 and oflags == 0
+
+
 def test_full_4096_rows_contiguous_e4m3_sampled():
     c = W.prefill_case("prefill_4096_e4m3", R=4096, n_sel=512, seed=6, first_block=4096,
                        kv_len=32768, interleaved=False, kv_dtype="e4m3")
@@ -198,3 +219,13 @@ def test_graph_replay_equals_eager(route):
     assert torch.equal(eager.view(torch.int16), out.view(torch.int16))
     want, _, _ = U.oracle_prefill(c)
     U.assert_close(out.cpu().numpy(), want, c.name)
+
+
+def test_grouped_route_long_sequence():
+    """A ~99,800-token sequence (a 780-word union bitmap, close to the
+    131,072-token limit of the grouped route): 48 rows near the end, each
+    with 256 selections spread over ~25,000 earlier blocks."""
+    c = _small(210, R=48, n_sel=256, first_block=24900, tails=(1, 2, 3))
+    assert c.kv_len > 99000
+    _check_full(c, dict(route=2))
+    _check_full(c, dict(route=2, rows_per_group=21))
