@@ -229,3 +229,25 @@ def test_grouped_route_long_sequence():
     assert c.kv_len > 99000
     _check_full(c, dict(route=2))
     _check_full(c, dict(route=2, rows_per_group=21))
+
+
+@pytest.mark.parametrize("route", ROUTES, ids=ROUTE_IDS)
+def test_degenerate_inputs(route):
+    """Every row empty (q_pos < 0), a zero-length sequence, every selection
+    padding, and every page of the table invalid: outputs are zero or the
+    tail alone, flags as the oracle's."""
+    c = _small(220, R=9)
+    c.q_pos[:] = -1                                            # all rows empty
+    got = _check_full(c, route)
+    assert np.all(got == 0)
+    c = _small(221, R=9)
+    c.kv_len = 0                                               # no tokens at all
+    got = _check_full(c, route)
+    assert np.all(got == 0)
+    c = _small(222, R=9)
+    c.sel_idx[:] = -1                                          # tails only
+    _check_full(c, route)
+    c = _small(223, R=9)
+    c.block_table[:] = -5                                      # every page invalid
+    got = _check_full(c, route)
+    assert np.all(got == 0)
