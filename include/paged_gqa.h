@@ -212,8 +212,10 @@ int paged_gqa_sparse_prefill(const void* q, const void* k_cache, const void* v_c
                              void* out, int* err_flag, void* stream);
 
 /*
- * paged_gqa_sparse_prefill with the kernel route chosen by the caller (for
- * testing and comparing the two designs; results agree within rounding):
+ * paged_gqa_sparse_prefill with the kernel route chosen by the caller: the
+ * same operation ("[Kernel][SM70] Accelerate Qwen3.8 QSA paged prefill",
+ * Changes), arguments, layouts, inert rules and flags, computed by one of
+ * two designs whose results agree within rounding:
  *  route = PAGED_GQA_PREFILL_AUTO     grouped when kv_len <= 131072 and
  *                                     32 * n_sel >= kv_len (FP16) or
  *                                     16 * n_sel >= kv_len (E4M3): dense
@@ -235,16 +237,6 @@ int paged_gqa_sparse_prefill(const void* q, const void* k_cache, const void* v_c
  * A listed block counts once per listing on both routes (duplicates are a
  * caller error; the grouped route recounts such rows on a slow path).
  */
-/*
- * Rows per group of the grouped route for R query rows of Hq / Hkv heads on
- * the current device, given rows_per_group as passed to
- * paged_gqa_sparse_prefill_route (0 = automatic: groups sized so the units
- * fill whole waves of one CTA per SM).  Returns the count, or a negative
- * status: PAGED_GQA_ERR_SHAPE (R < 1, Hq % Hkv != 0, rows_per_group out of
- * range), PAGED_GQA_ERR_UNSUPPORTED (more than 8 query heads per KV head),
- * PAGED_GQA_ERR_CUDA (no device to query).  Host only; launches nothing.
- */
-int paged_gqa_sparse_prefill_group_rows(int R, int Hq, int Hkv, int rows_per_group);
 
 #define PAGED_GQA_PREFILL_AUTO     0
 #define PAGED_GQA_PREFILL_ROWWISE  1
@@ -257,6 +249,19 @@ int paged_gqa_sparse_prefill_route(const void* q, const void* k_cache, const voi
                                    float kv_scale, float softmax_scale,
                                    void* out, int* err_flag, void* stream,
                                    int route, int rows_per_group);
+
+/*
+ * Rows per group of the grouped route for R query rows of Hq / Hkv heads on
+ * the current device, given rows_per_group as passed to
+ * paged_gqa_sparse_prefill_route (0 = automatic: groups sized so the units
+ * fill whole waves of one CTA per SM).  Returns the count, or a negative
+ * status: PAGED_GQA_ERR_SHAPE (R < 1, Hq % Hkv != 0, rows_per_group out of
+ * range), PAGED_GQA_ERR_UNSUPPORTED (more than 8 query heads per KV head),
+ * PAGED_GQA_ERR_CUDA (no device to query).  Host only; launches nothing.
+ * The pages have no counterpart of this helper: it tells a caller how the
+ * grouped route partitions its rows (for sizing benchmarks and reports).
+ */
+int paged_gqa_sparse_prefill_group_rows(int R, int Hq, int Hkv, int rows_per_group);
 
 /*
  * QSA block selection ("[Kernel][SM70] Accelerate exact Qwen3.8 decode",
