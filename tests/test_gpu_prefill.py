@@ -251,3 +251,13 @@ def test_degenerate_inputs(route):
     c.block_table[:] = -5                                      # every page invalid
     got = _check_full(c, route)
     assert np.all(got == 0)
+
+
+@pytest.mark.parametrize("Hq,Hkv,rows", [(2, 2, 128), (2, 2, 0), (6, 2, 42), (3, 1, 0)])
+def test_grouped_route_head_groupings(Hq, Hkv, rows):
+    """One query head per KV head (128 rows per group: 32 mask words per row,
+    64 stages per mask window, so a union of ~130 stages is masked in three
+    windows), three per KV head, two KV heads; forced and automatic group
+    sizes."""
+    c = _small(230 + Hq + Hkv + rows, R=150, n_sel=256, first_block=2000, Hq=Hq, Hkv=Hkv)
+    _check_full(c, dict(route=2, rows_per_group=rows))
