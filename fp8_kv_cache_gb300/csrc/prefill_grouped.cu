@@ -17,24 +17,27 @@
 //   * setup: the rows' valid entries are OR-ed into a bitmap over the
 //     sequence's blocks; a prefix popcount ranks the union; each row gets a
 //     16-bit mask per 64-token stage saying which of the stage's 16 blocks it
-//     attends (its own block limited to positions <= p).
-//   * 8 producer warps gather stage after stage (K of half-tile m+1, then V
-//     of m) with 16-byte cp.async into a 4-stage ring, laid out as the
-//     128-byte-swizzled K-major tile (see tc_device.cuh).
-//   * one thread issues S = Q K^T (M = 128 slots, N = 64 tokens, K = 256;
-//     Q and K from shared memory) into a TMEM buffer, and O += P V (M = 128,
-//     N = 256, K = 64; P from TMEM, V from the same ring bytes as an MN-major
-//     operand) into a 256-column TMEM accumulator.
-//   * 4 softmax warps own one slot each per thread: they read the slot's 64
-//     scores from TMEM, mask them, keep the running max and sum, write the
-//     FP16 probabilities back over the scores (two S/P buffers alternate), and
-//     rescale O in TMEM only when a running max grows by more than 2^8 (the
-//     sum and O always share one reference max, so the result is exact up to
-//     rounding).
+//     attends (its own block limited to positions <= p); Q goes to TMEM.
+//   * 5 producer warps, one per slot of a 5-stage ring, gather whole stages
+//     (K and V of 64 tokens, in the order K0 K1 K2 V0 K3 V1 ...) into the
+//     128-byte-swizzled K-major tile (see tc_device.cuh): FP16 rows by 16-byte
+//     cp.async, E4M3 rows through registers and the hardware converter.
+//   * one thread issues S = Q K^T (M = 128 slots, N = 64 tokens, K = 256; Q
+//     from TMEM, K from the stage) into one of two TMEM score buffers, two
+//     stages ahead of O += P V (M = 128, N = 256, K = 64; P from shared
+//     memory, V from the stage bytes read as an MN-major operand) into a
+//     256-column TMEM accumulator.
+//   * 8 softmax warps, two per TMEM lane quarter, take 32 of a slot's 64
+//     score columns each: they read the scores (freeing the buffer for the
+//     next Q K^T), mask them, agree on the stage maximum through shared
+//     memory, keep a running reference that O is rescaled to (in TMEM) only
+//     when it grows by more than 2^8 (the sum and O always share one
+//     reference, so the result is exact up to rounding), and write FP16
+//     probabilities for P V.
 // Masked-out (slot, token) pairs cost tensor-core work but no memory traffic;
-// on the 4096-row workload the union is about 0.6 of the per-row gather.
-// Groups are sized so the units fill whole waves of one CTA per SM and are
-// dealt in snake order (later rows have longer prefixes).
+// on the 4096-row workload the union is 0.60 of the per-row gather.  Groups
+// are sized so the units fill whole waves of one CTA per SM and are dealt in
+// snake order (later rows have longer prefixes).
 //
 // Duplicated selections (a caller error) keep their meaning -- a block listed
 // c times counts c times -- through a slow per-row recount.
@@ -157,9 +160,10 @@ __device__ __forceinline__ int block_of_rank(const Smem& sm, int nbw, int k)
     return 32 * lo + (int)__fns(sm.bitmap[lo], 0, k - sm.rank[lo] + 1);
 }
 
-// Stage masks of the half-tiles [ht0, ht0 + cap) for every row of the group,
-// built by the 128 softmax threads (named barrier 1).  A block already
-// present in a row's mask is a duplicated selection: the row is marked.
+// Stage masks of the half-tiles (64-token tiles: one K and one V stage each)
+// [ht0, ht0 + cap) for every row of the group, built by the 256 softmax
+// threads (named barrier 1).  A block already present in a row's mask is a
+// duplicated selection: the row is marked.
 __device__ void build_masks(const GroupArgs& ga, Smem& sm, int r0, int Rg, int ht0, int cap,
                             int words_per_row)
 {
