@@ -19,7 +19,9 @@ four-token blocks + a 1..3-token tail, Hq6/Hkv1/D256 FP16, interleaved K/V,
 32768-token cache) timed the same way, the same prefill over an E4M3 copy of
 the cache, the same FP16 rows on the grouped tcgen05 route (union of each row
 group's blocks gathered once; its gathered bytes and tensor-core rate), both
-prefill routes on denser selections (2048 blocks per row), the QSA block selection that produces such selections (4096 rows
+prefill routes on denser selections (2048 blocks per row), the B=8 x 1024-token
+E4M3 decode (16 MiB of KV: read from HBM after the flush, but too small to
+stream at the HBM rate), the QSA block selection that produces such selections (4096 rows
 of 8192 block scores, k = 512), the decode step's top-k/top-p masking of
 16 x 248,320 logits (k = 20, p = 0.95), the roofline of the dominant kernel
 (the decode split kernel, timed by CUDA events the library records around it
@@ -98,8 +100,8 @@ def measured_bf16_tflops():
 
 
 # Sources the decode split kernel is compiled from; its ncu traffic figure is
-# tied to their hash.
-DECODE_SOURCES = ("decode.cu", "pgqa_device.cuh", "pgqa_internal.h")
+# tied to their hash (and to its argument block in pgqa_internal.h).
+DECODE_SOURCES = ("decode.cu", "pgqa_device.cuh")
 
 
 def source_hash() -> str:
@@ -109,6 +111,10 @@ def source_hash() -> str:
     for name in DECODE_SOURCES:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
+    with open(os.path.join(csrc, "pgqa_internal.h")) as f:
+        internal = f.read()
+    start = internal.index("struct DecodeArgs {")
+    h.update(internal[start:internal.index("};", start)].encode())
     return h.hexdigest()[:16]
 
 
@@ -438,6 +444,19 @@ def run_ours(args, rank, world):
     m_out = torch.empty_like(m_x)
     m_ms = time_phase(lambda: P.paged_gqa_topk_topp_mask(m_x, mc_.k, mc_.p, out=m_out))
     m_bytes = 2 * mc_.logits.nbytes                            # the logits read once, written once
+    # ---- the B=8 x 1024-token E4M3 decode (16 MiB of KV), from HBM after an
+    # L2 flush like every timed call here
+    c8 = W.e4m3_b8()
+    kv8 = torch.from_numpy(c8.kv).to(dev)
+    q8, bt8 = torch.from_numpy(c8.q).to(dev), torch.from_numpy(c8.block_table).to(dev)
+    sl8, out8 = torch.from_numpy(c8.seq_lens).to(dev), torch.empty((c8.B, c8.Hq, c8.D),
+                                                                   dtype=torch.float16, device=dev)
+    ws8 = torch.empty(P.paged_gqa_decode_workspace_size(c8.B, c8.Hq, c8.Hkv, c8.D, c8.max_seq_len),
+                      dtype=torch.uint8, device=dev)
+    b8_ms = time_phase(lambda: P.paged_gqa_decode(
+        q8, kv8[0], kv8[1], bt8, sl8, c8.page_size, c8.kv_scale, c8.softmax_scale, out8,
+        max_seq_len=c8.max_seq_len, workspace=ws8))
+    kvb8 = decode_kv_bytes(c8)
     clocks.stop()
     s_rows = sc.scores.shape[0]
     s_cands = int(np.minimum(sc.q_pos.astype(np.int64) // 4, sc.n_blocks).sum())
@@ -525,6 +544,13 @@ def run_ours(args, rank, world):
             "algorithmic_bytes": s_bytes,
             "GBps": round(s_bytes / (s_ms * 1e-3) / 1e9, 1),
             "hbm_frac": round(s_bytes / (s_ms * 1e-3) / 1e9 / peak, 4),
+        },
+        "decode_e4m3_b8_l1024": {
+            "workload": "FP8-E4M3 KV decode: B=8, Hkv=4, Hq=24, D=256, 1024 tokens each, page 16, "
+                        "shuffled 512-page pool (16 MiB of KV, read from HBM after an L2 flush)",
+            "us": round(b8_ms * 1e3, 2), "tok_s": round(world * c8.B / (b8_ms * 1e-3), 1),
+            "kv_bytes": kvb8, "GBps": round(kvb8 / (b8_ms * 1e-3) / 1e9, 1),
+            "hbm_frac": round(kvb8 / (b8_ms * 1e-3) / 1e9 / peak, 4),
         },
         "topk_topp_mask": {
             "workload": "16 rows of 248,320 float32 logits, top-k 20 then top-p 0.95, "
