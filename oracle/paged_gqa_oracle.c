@@ -37,7 +37,7 @@
  * or E4M3 code -> E(c) * kv_scale in FP64 (exact: a 4-bit significand times a
  * 24-bit one fits in 53 bits).
  *
- * Readings taken where the pages are silent (each is listed in the design doc):
+ * Readings taken where the pages are silent:
  *   - query head h uses KV head floor(h / G), G = Hq / Hkv (consecutive groups);
  *   - one kv_scale per call multiplies both K and V codes; unused for FP16;
  *   - E4M3 is the OCP E4M3FN variant: no infinities, codes 0x7F/0xFF are NaN,
@@ -462,7 +462,7 @@ int64_t orc_sparse_row_tokens(const int32_t* block_table, int num_pages, int kv_
  * the first min(k, n), and list them by increasing block index, padded with
  * -1 to k entries.
  *
- * Readings taken where the pages are silent (listed in the design doc):
+ * Readings taken where the pages are silent:
  *   - the candidates of a row at position p are the blocks strictly before its
  *     own block, 0 .. floor(p / 4) - 1, the blocks [P] accepts in a selection;
  *     p is q_pos clamped to kv_len - 1 as in [P] (ORC_FLAG_QPOS_CLAMPED);
@@ -580,7 +580,7 @@ int orc_select_blocks(const float* scores, int64_t score_stride, int n_blocks,
  * reaches p, the probabilities being the softmax over the top-k logits; every
  * logit not kept becomes -infinity, kept logits pass through unchanged.
  *
- * Readings taken where the pages are silent (listed in the design doc):
+ * Readings taken where the pages are silent:
  *   - top-k keeps exactly min(k, V) logits, ties to the lower index;
  *   - the top-p mass is computed in FP64: e_j = exp(x_j - x_0) over the
  *     top-k list in order (x_0 its largest), suffix sums S_j = e_j + S_{j+1}
