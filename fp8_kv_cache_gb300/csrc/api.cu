@@ -276,7 +276,7 @@ int paged_gqa_sparse_prefill_route(const void* q, const void* k_cache, const voi
     a.v_scale = e4m3 ? kv_scale : 1.f;
     a.out = static_cast<__half*>(out);
     a.err = err_flag;
-    const bool grouped_ok = grouped_prefill_supported(a, e4m3);
+    const bool grouped_ok = grouped_prefill_supported(a);
     if (route == PAGED_GQA_PREFILL_GROUPED && !grouped_ok)
         return PAGED_GQA_ERR_UNSUPPORTED;
     if (rows_per_group > kGroupSlots / a.G)

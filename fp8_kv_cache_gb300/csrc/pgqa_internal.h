@@ -95,7 +95,7 @@ int split_ctas_per_sm(bool e4m3);
 
 cudaError_t launch_decode(const DecodeArgs& a, bool e4m3, cudaStream_t s, void* ev0, void* ev1);
 cudaError_t launch_prefill(const PrefillArgs& a, bool e4m3, cudaStream_t s);
-bool grouped_prefill_supported(const PrefillArgs& a, bool e4m3);
+bool grouped_prefill_supported(const PrefillArgs& a);
 int grouped_prefill_rows(const PrefillArgs& a, int sms, int rows_per_group);
 cudaError_t launch_prefill_grouped(const PrefillArgs& a, bool e4m3, int rows_per_group,
                                    cudaStream_t s);

@@ -715,7 +715,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_prefill_grouped_kernel(con
 
 }  // namespace grp
 
-bool grouped_prefill_supported(const PrefillArgs& a, bool)
+bool grouped_prefill_supported(const PrefillArgs& a)
 {
     return a.G >= 1 && a.G <= grp::kM &&
            (int64_t)a.kv_len <= (int64_t)4 * 32 * kGroupMaxWords;
