@@ -27,7 +27,8 @@ __all__ = [
     "PagedGQAError", "library_path", "lib", "KV_FP16", "KV_E4M3",
     "FLAG_BAD_PAGE", "FLAG_SEQ_CLAMPED", "FLAG_EMPTY_ROW", "FLAG_QPOS_CLAMPED", "FLAG_BAD_SEL",
     "paged_gqa_decode", "paged_gqa_decode_noalloc", "paged_gqa_sparse_prefill",
-    "paged_gqa_sparse_prefill_route", "paged_gqa_sparse_prefill_group_rows", "PREFILL_AUTO", "PREFILL_ROWWISE", "PREFILL_GROUPED",
+    "paged_gqa_sparse_prefill_route", "paged_gqa_sparse_prefill_group_rows", "PREFILL_AUTO",
+    "PREFILL_ROWWISE", "PREFILL_GROUPED", "paged_gqa_debug_grouped_prefill_stall",
     "paged_gqa_gather_dequant",
     "paged_gqa_sparse_prefill_tokens", "paged_gqa_decode_workspace_size",
     "paged_gqa_decode_workspace_size_splits",
@@ -106,6 +107,10 @@ def lib():
                                                          vp, i32, vp, i32, i32, i32, i32, i32,
                                                          f32, f32, vp, vp, vp, i32, i32]
             L.paged_gqa_sparse_prefill_route.restype = i32
+            L.paged_gqa_debug_grouped_prefill_stall.argtypes = [
+                vp, vp, vp, KVLayout, i32, vp, i32, i32, vp, i32, vp, i32, i32, i32, i32, i32,
+                f32, f32, vp, vp, vp, ctypes.c_longlong, i32]
+            L.paged_gqa_debug_grouped_prefill_stall.restype = i32
             L.paged_gqa_sparse_prefill_group_rows.argtypes = [i32, i32, i32, i32]
             L.paged_gqa_sparse_prefill_group_rows.restype = i32
             L.paged_gqa_gather_dequant.argtypes = [vp, KVLayout, i32, vp, i64, vp, i32, i32, i32,
@@ -272,6 +277,21 @@ def paged_gqa_sparse_prefill_route(q, k_cache, v_cache, block_table, kv_len, sel
                               page_size, softmax_scale, kv_scale, out, num_pages, err_flag, stream)
     _check(lib().paged_gqa_sparse_prefill_route(*args, int(route), int(rows_per_group)),
            "paged_gqa_sparse_prefill_route")
+    return out
+
+
+def paged_gqa_debug_grouped_prefill_stall(q, k_cache, v_cache, block_table, kv_len, sel_idx,
+                                          q_pos, page_size, softmax_scale, kv_scale=1.0,
+                                          out=None, *, spin_limit, stall_stage, num_pages=None,
+                                          err_flag=None, stream=None):
+    """Test hook of the grouped route's time-out path: every bounded wait
+    gives up after ``spin_limit`` polls and each CTA leaves ring stage
+    ``stall_stage`` unpublished (-1: none), so the kernel sets FLAG_TIMEOUT
+    and leaves ``out`` undefined.  For tests of that path only."""
+    args, out = _prefill_args(q, k_cache, v_cache, block_table, kv_len, sel_idx, q_pos,
+                              page_size, softmax_scale, kv_scale, out, num_pages, err_flag, stream)
+    _check(lib().paged_gqa_debug_grouped_prefill_stall(*args, int(spin_limit), int(stall_stage)),
+           "paged_gqa_debug_grouped_prefill_stall")
     return out
 
 

@@ -109,6 +109,14 @@ int check_decode_shape(int B, int Hq, int Hkv, int D, int max_seq_len)
     return PAGED_GQA_OK;
 }
 
+int prefill_route_impl(const void* q, const void* k_cache, const void* v_cache,
+                       paged_gqa_kv_layout kv_layout, int kv_dtype, const int32_t* block_table,
+                       int num_pages, int kv_len, const int32_t* sel_idx, int n_sel,
+                       const int32_t* q_pos, int R, int Hq, int Hkv, int D, int page_size,
+                       float kv_scale, float softmax_scale, void* out, int* err_flag,
+                       void* stream, int route, int rows_per_group, long spin_limit,
+                       int stall_stage);
+
 }  // namespace
 
 extern "C" {
@@ -238,6 +246,40 @@ int paged_gqa_sparse_prefill_route(const void* q, const void* k_cache, const voi
                                    float softmax_scale, void* out, int* err_flag, void* stream,
                                    int route, int rows_per_group)
 {
+    return prefill_route_impl(q, k_cache, v_cache, kv_layout, kv_dtype, block_table, num_pages,
+                              kv_len, sel_idx, n_sel, q_pos, R, Hq, Hkv, D, page_size, kv_scale,
+                              softmax_scale, out, err_flag, stream, route, rows_per_group, 0, -1);
+}
+
+int paged_gqa_debug_grouped_prefill_stall(const void* q, const void* k_cache, const void* v_cache,
+                                          paged_gqa_kv_layout kv_layout, int kv_dtype,
+                                          const int32_t* block_table, int num_pages, int kv_len,
+                                          const int32_t* sel_idx, int n_sel, const int32_t* q_pos,
+                                          int R, int Hq, int Hkv, int D, int page_size,
+                                          float kv_scale, float softmax_scale, void* out,
+                                          int* err_flag, void* stream, long long spin_limit,
+                                          int stall_stage)
+{
+    if (spin_limit < 0 || spin_limit > (1LL << 30) || stall_stage < -1)
+        return PAGED_GQA_ERR_SHAPE;
+    return prefill_route_impl(q, k_cache, v_cache, kv_layout, kv_dtype, block_table, num_pages,
+                              kv_len, sel_idx, n_sel, q_pos, R, Hq, Hkv, D, page_size, kv_scale,
+                              softmax_scale, out, err_flag, stream, PAGED_GQA_PREFILL_GROUPED, 0,
+                              (long)spin_limit, stall_stage);
+}
+
+}  // extern "C"
+
+namespace {
+
+int prefill_route_impl(const void* q, const void* k_cache, const void* v_cache,
+                       paged_gqa_kv_layout kv_layout, int kv_dtype, const int32_t* block_table,
+                       int num_pages, int kv_len, const int32_t* sel_idx, int n_sel,
+                       const int32_t* q_pos, int R, int Hq, int Hkv, int D, int page_size,
+                       float kv_scale, float softmax_scale, void* out, int* err_flag,
+                       void* stream, int route, int rows_per_group, long spin_limit,
+                       int stall_stage)
+{
     if (route < PAGED_GQA_PREFILL_AUTO || route > PAGED_GQA_PREFILL_GROUPED ||
         rows_per_group < 0)
         return PAGED_GQA_ERR_SHAPE;
@@ -293,10 +335,15 @@ int paged_gqa_sparse_prefill_route(const void* q, const void* k_cache, const voi
                          (route == PAGED_GQA_PREFILL_AUTO && grouped_ok &&
                           density * n_sel >= (int64_t)kv_len);
     const cudaError_t e =
-        grouped ? launch_prefill_grouped(a, e4m3, rows_per_group, static_cast<cudaStream_t>(stream))
+        grouped ? launch_prefill_grouped(a, e4m3, rows_per_group, static_cast<cudaStream_t>(stream),
+                                         spin_limit, stall_stage)
                 : launch_prefill(a, e4m3, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PAGED_GQA_OK : PAGED_GQA_ERR_CUDA;
 }
+
+}  // namespace
+
+extern "C" {
 
 int paged_gqa_sparse_prefill_group_rows(int R, int Hq, int Hkv, int rows_per_group)
 {
@@ -421,3 +468,21 @@ int paged_gqa_topk_topp_mask(const float* logits, int64_t logits_stride, float* 
 }
 
 }  // extern "C"
+
+namespace pgqa {
+
+// Workspace bytes paged_gqa_decode needs for this shape with its automatic
+// split count on the current device for the given KV dtype (0 when the shape
+// is invalid or takes the unsplit route).
+size_t decode_workspace_bytes_for(int B, int Hq, int Hkv, int D, int kv_dtype)
+{
+    if (check_decode_shape(B, Hq, Hkv, D, 0) != PAGED_GQA_OK || B > kMaxSplitBatch)
+        return 0;
+    DeviceInfo di;
+    if (device_info(di) != PAGED_GQA_OK)
+        return 0;
+    const int per = kv_dtype == PAGED_GQA_KV_E4M3 ? di.ctas_e4m3 : di.ctas_fp16;
+    return workspace_bytes(B, Hkv, di.sms * per);
+}
+
+}  // namespace pgqa

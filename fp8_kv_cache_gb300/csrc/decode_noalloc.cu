@@ -11,13 +11,19 @@
 // allocating library routine).
 //
 // The array costs kNoAllocScratchBytes (16 MiB) of device memory on every GPU
-// that loads this library, for the life of the process.  Every call shares
-// it, so calls whose kernels could overlap on the GPU (for example on two
-// streams without ordering between them) race on it; calls on one stream, or
-// otherwise ordered, are safe.  Nothing in it has to start at zero: each call
-// writes every scratch value it later reads (the tile prefix, the split
-// count and the partial results it merges), so the contents a previous call
-// left behind are never read.
+// where this library's device code is loaded, for the life of the process.
+// With the CUDA runtime's lazy module loading (its default), that happens on
+// the first call of this entry point on each device, inside the address
+// lookup below: that first call is where the driver reserves the 16 MiB, so
+// it can fail for lack of memory and can synchronise.  Callers should make
+// one warm-up call per device at initialisation, before any stream capture
+// and outside any hook where allocation is forbidden; later calls allocate
+// nothing.  Every call shares the array, so calls whose kernels could
+// overlap on the GPU (for example on two streams without ordering between
+// them) race on it; calls on one stream, or otherwise ordered, are safe.
+// Nothing in it has to start at zero: each call writes every scratch value
+// it later reads (the tile prefix, the split count and the partial results
+// it merges), so the contents a previous call left behind are never read.
 #include <atomic>
 
 #include "pgqa_internal.h"
@@ -60,10 +66,11 @@ extern "C" int paged_gqa_decode_noalloc(const void* q, const void* k_cache, cons
                                         float kv_scale, float softmax_scale, void* out,
                                         int* err_flag, void* stream)
 {
-    // Shapes whose split scratch would not fit the static array are refused
-    // before anything is looked up or launched.
+    // Shapes whose split scratch, for this KV dtype, would not fit the
+    // static array are refused before anything is looked up or launched
+    // (paged_gqa_decode checks the same size again before its launches).
     if (B > 0) {
-        const size_t need = paged_gqa_decode_workspace_size(B, Hq, Hkv, D, max_seq_len);
+        const size_t need = pgqa::decode_workspace_bytes_for(B, Hq, Hkv, D, kv_dtype);
         if (need > kNoAllocScratchBytes)
             return PAGED_GQA_ERR_WORKSPACE;
     }

@@ -1,20 +1,26 @@
 // pgqa_device.cuh -- device building blocks of the paged GQA kernels (sm_103a).
 //
 // Data path of one warp, per tile of 16 tokens of one KV head:
-//   block table -> row addresses (lanes 0..15, one token each, shared by shuffles)
-//   -> 16-byte read-only global loads straight into registers
+//   block table -> row addresses (lanes 0..7 resolve one token each of a
+//   half-tile of 8; the offsets are shared by shuffles)
+//   -> 16-byte cp.async.cg copies (global -> shared, bypassing L1) into the
+//      warp's private ring of half-tile stages (WarpRing below), kNS - 2
+//      half-tiles in flight while the current tile is computed; chunks are
+//      XOR-swizzled in the stage so the fragment reads are conflict-free
+//   -> 16-byte shared-memory loads of the K and V rows into registers
 //   -> in-register E4M3 -> f16x2 conversion (hardware cvt) or FP16 as is
-//   -> S = Q K^T on the tensor cores (mma.sync m16n8k16, f16 in, f32 accumulate;
-//      rows = the group's query heads, padded to 16; columns = 8 tokens)
-//   -> online softmax in f32 (log2 domain, 4-lane shuffles per head)
+//   -> S^T = K Q^T on the tensor cores (mma.sync m16n8k16, f16 in, f32
+//      accumulate; rows = the 16 tokens, columns = the group's query heads,
+//      padded to 8; Q's fragments are staged once per piece in shared memory)
+//   -> online softmax in f32 (log2 domain, shuffles across the 8 lane groups)
 //   -> O^T += V^T P^T on the tensor cores (rows = head-dim slots, columns = the
 //      8 padded heads, k = 16 tokens) plus one extra MMA against a ones matrix
 //      that yields the softmax denominator from the same FP16 probabilities.
-// The fragments are arranged so that no shared memory is touched on the way:
-//   * the head-dim reduction order is free, so each lane loads contiguous
-//     16-byte chunks and Q's fragments are permuted to match;
-//   * the C fragment of S (rows heads, columns tokens 2q, 2q+1) is exactly the
-//     B fragment P^T needs for the second MMA;
+// The fragments are arranged so that no data moves between lanes on the way:
+//   * the head-dim reduction order is free, so each lane reads contiguous
+//     16-byte chunks of a row and Q's fragments are permuted to match;
+//   * two movmatrix transposes turn the probabilities of S^T's C fragment
+//     into the B fragment P^T the second MMA needs;
 //   * V's token pairs are interleaved with one byte permute per register.
 //
 // The operation is the paged GQA attention of "[Kernel][SM70] Scale NVFP4 E4M3

@@ -65,6 +65,8 @@ struct GroupArgs {
     int Rg;              // query rows per group (unit = group x KV head)
     int n_units;
     int nbw;             // words of the union bitmap
+    long spin_limit;     // polls of a bounded wait before it gives up
+    int stall_stage;     // test hook: ring stage never published (-1: none)
 };
 
 struct SelectArgs {
@@ -91,6 +93,7 @@ struct MaskArgs {
 
 size_t decode_split_smem(bool e4m3, int B);
 size_t workspace_bytes(int B, int Hkv, int C);
+size_t decode_workspace_bytes_for(int B, int Hq, int Hkv, int D, int kv_dtype);
 int split_ctas_per_sm(bool e4m3);
 
 cudaError_t launch_decode(const DecodeArgs& a, bool e4m3, cudaStream_t s, void* ev0, void* ev1);
@@ -98,7 +101,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, bool e4m3, cudaStream_t s);
 bool grouped_prefill_supported(const PrefillArgs& a);
 int grouped_prefill_rows(const PrefillArgs& a, int sms, int rows_per_group);
 cudaError_t launch_prefill_grouped(const PrefillArgs& a, bool e4m3, int rows_per_group,
-                                   cudaStream_t s);
+                                   cudaStream_t s, long spin_limit = 0, int stall_stage = -1);
 cudaError_t launch_gather(const KVGeom& g, bool e4m3, const int32_t* bt, int64_t bt_stride,
                           const int32_t* seq_lens, int B, int T, int Hkv, int max_seq_len,
                           float kv_scale, float* out, cudaStream_t s);

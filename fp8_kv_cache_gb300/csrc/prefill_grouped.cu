@@ -23,17 +23,23 @@
 //     128-byte-swizzled K-major tile (see tc_device.cuh): FP16 rows by 16-byte
 //     cp.async, E4M3 rows through registers and the hardware converter.
 //   * one thread issues S = Q K^T (M = 128 slots, N = 64 tokens, K = 256; Q
-//     from TMEM, K from the stage) into one of two TMEM score buffers, two
-//     stages ahead of O += P V (M = 128, N = 256, K = 64; P from shared
-//     memory, V from the stage bytes read as an MN-major operand) into a
-//     256-column TMEM accumulator.
-//   * 8 softmax warps, two per TMEM lane quarter, take 32 of a slot's 64
-//     score columns each: they read the scores (freeing the buffer for the
-//     next Q K^T), mask them, agree on the stage maximum through shared
-//     memory, keep a running reference that O is rescaled to (in TMEM) only
-//     when it grows by more than 2^8 (the sum and O always share one
-//     reference, so the result is exact up to rounding), and write FP16
-//     probabilities for P V.
+//     from TMEM, K from the stage) into one of two TMEM score buffers as soon
+//     as a buffer is free, and a thread of another warp issues O += P V
+//     (M = 128, N = 256, K = 64; P from shared memory, V from the stage bytes
+//     read as an MN-major operand) into a 256-column TMEM accumulator once a
+//     stage's probabilities are written, so Q K^T runs ahead of the softmax
+//     without waiting behind P V.
+//   * 8 softmax warps in two warpgroups that take alternate stages (A the
+//     even ones, B the odd ones), so one group's exponentials and stores
+//     overlap the other's score reads.  A thread owns one slot (its TMEM
+//     lane) and all 64 score columns of its group's stage: it reads the
+//     scores (freeing the buffer for the next Q K^T), masks them, and takes
+//     the running reference maximum from the other group's previous stage
+//     (a named-barrier handoff per lane quarter, the only link between the
+//     groups).  The reference grows only when a stage's maximum exceeds it
+//     by more than 2^8, and then O is rescaled in TMEM; each group keeps its
+//     own sum under the reference it last saw, so the result is exact up to
+//     rounding.  FP16 probabilities go to shared memory for P V.
 // Masked-out (slot, token) pairs cost tensor-core work but no memory traffic;
 // on the 4096-row workload the union is 0.60 of the per-row gather.  Groups
 // are sized so the units fill whole waves of one CTA per SM and are dealt in
@@ -58,7 +64,9 @@ constexpr int kRegionBytes = kStageTokens * 128;      // 64 head-dim columns of 
 constexpr int kStageBytes = kStageTokens * kD * 2;    // 32 KB
 constexpr int kMaskWords = 4096;             // 16 KB of per-row stage masks
 constexpr int kSoftWarps = 8, kMmaWarp = 8, kProdWarps = kNS, kProdWarp0 = 9;
-constexpr int kThreads = 32 * (kSoftWarps + 1 + kProdWarps);
+constexpr int kPvWarp = kProdWarp0 + kProdWarps;   // issues P V; kMmaWarp issues Q K^T
+constexpr int kThreads = 32 * (kSoftWarps + 1 + kProdWarps + 1);
+constexpr int kGroupThreads = kSoftWarps / 2 * 32;   // one softmax warpgroup
 constexpr float kRescaleSlack = 8.f;         // log2-domain growth tolerated before rescaling O
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemQ = 0;               // Q: 128 columns of f16 pairs
@@ -73,12 +81,13 @@ struct Smem {
     int rank[kGroupMaxWords];                // exclusive prefix popcount of bitmap
     uint32_t masks[kMaskWords];              // [row][stage / 2]: two 16-bit stage masks per word
     int row_p[kM], row_own[kM], row_rank_own[kM], row_dup[kM];
-    float xm[2][2][kM];                      // [stage parity][half][slot]: stage maxima exchanged
-    float xl[2][kM];                         // [half][slot]: final sums exchanged
-    uint64_t full[kNS], empty[kNS];
+    float mref[kM];                          // [slot]: reference maximum handed between the groups
+    float xl[2][kM];                         // [group][slot]: final sums exchanged
+    uint64_t full_k[kNS], full_v[kNS], empty[kNS];   // K / V stage loaded, slot free
     uint64_t s_full[2], s_free[2], p_full[2], p_free[2], done;
     uint32_t tmem_base;
     int flags, n_union, abort;
+    long spin_limit;
 };
 
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;   // + alignment of the tiles
@@ -90,6 +99,15 @@ struct Cursor {
     uint32_t g = 0;     // half-tile (S/P buffer) counter
 };
 
+// Loaded stages of one kind (K or V) taken so far from each ring slot, by the
+// MMA thread that consumes that kind.  A slot's K and V occupants publish on
+// separate barriers (full_k, full_v), so each consumer waits for every phase
+// of its barriers in order: a parity wait is only unambiguous while its
+// barrier is at most one phase behind the phase waited for.
+struct SlotCount {
+    uint32_t n[kNS] = {0u, 0u, 0u, 0u, 0u};
+};
+
 // Bounded wait; after any wait of the CTA has timed out, waits are skipped
 // (every role keeps its control flow, so all barriers are still reached and
 // the kernel ends; the result is then garbage and PAGED_GQA_FLAG_TIMEOUT set).
@@ -98,7 +116,7 @@ __device__ __forceinline__ void wait_or_abort(Smem& sm, uint64_t* bar, uint32_t 
     volatile int* ab = &sm.abort;
     if (*ab)
         return;
-    if (!tc::mbar_wait(bar, par))
+    if (!tc::mbar_wait(bar, par, sm.spin_limit))
         *ab = 1;
 }
 
@@ -263,6 +281,11 @@ __device__ void unit_setup(const GroupArgs& ga, Smem& sm, int r0, int Rg, int j,
             sm.row_rank_own[tid] = rank_of_block(sm, own);
     }
     if (tid < kSoftWarps * 32) {             // Q into TMEM: lane = slot = (row slot / G, head slot % G)
+        // The softmax takes its scores in units of |score scale|: a negative
+        // scale is folded into Q by negating it, a zero scale by a zero Q
+        // (both exact), so that the kernel's score scale is positive.
+        const uint32_t q_xor = a.scale_log2 < 0.f ? 0x80008000u : 0u;
+        const uint32_t q_and = a.scale_log2 == 0.f ? 0u : 0xFFFFFFFFu;
         const int slot = tid & (kM - 1), half = tid >> 7;         // two threads per slot
         const int rl = slot / a.G, h = slot - rl * a.G;
         const bool live = rl < Rg && sm.row_own[rl] >= 0;
@@ -275,10 +298,10 @@ __device__ void unit_setup(const GroupArgs& ga, Smem& sm, int r0, int Rg, int j,
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
                 const uint4 v = live ? __ldg(src + 16 * half + 8 * part + c) : make_uint4(0u, 0u, 0u, 0u);
-                w[4 * c] = v.x;
-                w[4 * c + 1] = v.y;
-                w[4 * c + 2] = v.z;
-                w[4 * c + 3] = v.w;
+                w[4 * c] = (v.x ^ q_xor) & q_and;
+                w[4 * c + 1] = (v.y ^ q_xor) & q_and;
+                w[4 * c + 2] = (v.z ^ q_xor) & q_and;
+                w[4 * c + 3] = (v.w ^ q_xor) & q_and;
             }
             tc::tmem_st32(tl + kTmemQ + 64 * half + 32 * part, w);
         }
@@ -396,15 +419,51 @@ __device__ void produce(const GroupArgs& ga, Smem& sm, Cursor& cur, int j, int n
             cp_async_wait<0>();
         }
         tc::fence_async_shared();
-        tc::mbar_arrive(&sm.full[s]);
+        if ((int)cur.it != ga.stall_stage)   // test hook: a stage left unpublished
+            tc::mbar_arrive(is_v ? &sm.full_v[s] : &sm.full_k[s]);
     }
 }
 
-// The MMA thread, in stage order: Q K^T of half-tile m+2 goes out as soon as
-// the softmax has read S(m), before P V of m.
-__device__ void issue_mma(Smem& sm, Cursor& cur, int nt)
+// The two MMA issuer threads walk the unit's stages in ring order and each
+// acts on its own kind: Q K^T of a stage goes out as soon as its K stage is
+// full and its score buffer free (the softmax has read the scores two
+// stages back), independently of P V, which waits for the stage's
+// probabilities.  Both kinds share the tensor pipe; they touch disjoint TMEM
+// columns and shared-memory stages.
+__device__ void issue_qk(Smem& sm, Cursor& cur, SlotCount& taken, int nt)
 {
     constexpr uint32_t kIdQK = tc::f16_idesc(kM, kStageTokens, false, false);
+    const uint32_t tm = sm.tmem_base;
+    const uint32_t g0 = cur.g;
+    for (int q = 0; q < 2 * nt; ++q, ++cur.it) {
+        bool is_v;
+        int ht;
+        stage_of(q, nt, is_v, ht);
+        if (is_v)
+            continue;
+        const uint32_t g = g0 + ht, buf = g & 1, s = cur.it % kNS;
+        const uint32_t st = tc::smem_addr(sm.ring[s]);
+        wait_or_abort(sm, &sm.full_k[s], taken.n[s]++ & 1);
+        if (g >= 2)
+            wait_or_abort(sm, &sm.s_free[buf], ((g >> 1) - 1) & 1);
+        tc::fence_after_sync();
+        // descriptors advance by their 16-byte address field: K steps of
+        // 16 elements are 32 bytes inside a row, every 4th a new region
+        const uint64_t db0 = tc::sw128_desc(st, 16, 1024);
+        const uint32_t d = tm + kTmemS + 64 * buf;
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk)
+            tc::mma_ts(d, tm + kTmemQ + 8 * kk,
+                       db0 + (uint64_t)(((kk >> 2) * kRegionBytes + (kk & 3) * 32) >> 4), kIdQK,
+                       kk > 0);
+        tc::mma_commit(&sm.empty[s]);
+        tc::mma_commit(&sm.s_full[buf]);
+    }
+    cur.g = g0 + nt;
+}
+
+__device__ void issue_pv(Smem& sm, Cursor& cur, SlotCount& taken, int nt)
+{
     constexpr uint32_t kIdPV = tc::f16_idesc(kM, kD, false, true);
     const uint32_t tm = sm.tmem_base;
     const uint32_t g0 = cur.g;
@@ -412,37 +471,22 @@ __device__ void issue_mma(Smem& sm, Cursor& cur, int nt)
         bool is_v;
         int ht;
         stage_of(q, nt, is_v, ht);
+        if (!is_v)
+            continue;
         const uint32_t g = g0 + ht, buf = g & 1, s = cur.it % kNS;
         const uint32_t st = tc::smem_addr(sm.ring[s]);
-        wait_or_abort(sm, &sm.full[s], (cur.it / kNS) & 1);
-        if (!is_v) {
-            if (g >= 2)
-                wait_or_abort(sm, &sm.s_free[buf], ((g >> 1) - 1) & 1);
-            tc::fence_after_sync();
-            // descriptors advance by their 16-byte address field: K steps of
-            // 16 elements are 32 bytes inside a row, every 4th a new region
-            const uint64_t db0 = tc::sw128_desc(st, 16, 1024);
-            const uint32_t d = tm + kTmemS + 64 * buf;
+        wait_or_abort(sm, &sm.full_v[s], taken.n[s]++ & 1);
+        wait_or_abort(sm, &sm.p_full[buf], (g >> 1) & 1);
+        tc::fence_after_sync();
+        const uint64_t da0 = tc::sw128_desc(tc::smem_addr(sm.p[buf]), 16, 1024);
+        const uint64_t db0 = tc::sw128_desc(st, kRegionBytes, 1024);
+        const uint32_t acc0 = ht > 0;
 #pragma unroll
-            for (int kk = 0; kk < kD / 16; ++kk)
-                tc::mma_ts(d, tm + kTmemQ + 8 * kk,
-                           db0 + (uint64_t)(((kk >> 2) * kRegionBytes + (kk & 3) * 32) >> 4), kIdQK,
-                           kk > 0);
-            tc::mma_commit(&sm.empty[s]);
-            tc::mma_commit(&sm.s_full[buf]);
-        } else {
-            wait_or_abort(sm, &sm.p_full[buf], (g >> 1) & 1);
-            tc::fence_after_sync();
-            const uint64_t da0 = tc::sw128_desc(tc::smem_addr(sm.p[buf]), 16, 1024);
-            const uint64_t db0 = tc::sw128_desc(st, kRegionBytes, 1024);
-            const uint32_t acc0 = ht > 0;
-#pragma unroll
-            for (int kk = 0; kk < kStageTokens / 16; ++kk)
-                tc::mma_ss(tm + kTmemO, da0 + (uint64_t)(kk * 2), db0 + (uint64_t)(kk * 128), kIdPV,
-                           kk > 0 ? 1u : acc0);
-            tc::mma_commit(&sm.empty[s]);
-            tc::mma_commit(&sm.p_free[buf]);
-        }
+        for (int kk = 0; kk < kStageTokens / 16; ++kk)
+            tc::mma_ss(tm + kTmemO, da0 + (uint64_t)(kk * 2), db0 + (uint64_t)(kk * 128), kIdPV,
+                       kk > 0 ? 1u : acc0);
+        tc::mma_commit(&sm.empty[s]);
+        tc::mma_commit(&sm.p_free[buf]);
     }
     cur.g = g0 + nt;
 }
@@ -460,103 +504,186 @@ __device__ int listed_count(const PrefillArgs& a, int r, int b, int own)
     return c;
 }
 
-// Named barrier of the two softmax warps that share TMEM lane quarter wq.
-__device__ __forceinline__ void pair_sync(int wq)
+// Slow path of a row with duplicated selections: the probabilities of each
+// attended block of the stage (first union rank k0) in the slot's P row are
+// multiplied by the number of times the row lists the block; returns the
+// probability mass this adds to the row's sum.
+__device__ __noinline__ float scale_listed(const PrefillArgs& a, const Smem& sm,
+                                           unsigned char* prow, int slot, int r, int own, int nbw,
+                                           int k0, uint32_t live16)
 {
-    asm volatile("bar.sync %0, 64;" ::"r"(2 + wq) : "memory");
+    float added = 0.f;
+    for (int kb = 0; kb < kStageBlocks; ++kb) {
+        if (!((live16 >> kb) & 1u))
+            continue;
+        const int cnt = listed_count(a, r, block_of_rank(sm, nbw, k0 + kb), own);
+        if (cnt == 1)
+            continue;
+        __half2* h = reinterpret_cast<__half2*>(prow + (((kb >> 1) ^ (slot & 7)) << 4) +
+                                                8 * (kb & 1));
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const float2 f = __half22float2(h[e]);
+            const float p0 = f.x * (float)cnt, p1 = f.y * (float)cnt;
+            added += (p0 + p1) - (f.x + f.y);
+            h[e] = __floats2half2_rn(p0, p1);
+        }
+    }
+    return added;
 }
 
-// Softmax warps: slot = t & 127 (row slot / G, head slot % G) = TMEM lane;
-// half = t >> 7 takes score columns 32 half .. 32 half + 31 of each stage (the
-// warps of both halves on one lane quarter exchange the stage maximum through
-// shared memory), O columns 128 half .. 128 half + 127 when O is rescaled or
-// written, and writes P columns 16 half .. 16 half + 15.
+// Named barriers of the softmax warps (0 is __syncthreads, 1 the mask
+// rebuild of all softmax warps).  Per TMEM lane quarter wq: the reference
+// handoff from warpgroup A to B (2 + wq) and from B to A (6 + wq), and the
+// exchange of the sums at the end of a unit (10 + wq).
+__device__ __forceinline__ void named_sync(int id)
+{
+    asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory");
+}
+
+__device__ __forceinline__ void named_arrive(int id)
+{
+    asm volatile("bar.arrive %0, 64;" ::"r"(id) : "memory");
+}
+
+// Softmax warps.  Warpgroup wg = t >> 7 takes the unit's stages i = wg,
+// wg + 2, ...; slot = t & 127 (row slot / G, head slot % G) is the thread's
+// TMEM lane, and the thread handles all 64 score columns of its stage.  Per
+// stage:
+//   1. the scores (two 32-column TMEM loads; the buffer is then released),
+//      masked to the blocks the slot's row attends, and their maximum;
+//   2. the reference m after the previous stage, from the other group
+//      (named barrier); m grows to this stage's maximum only when that
+//      exceeds it by more than 2^8 -- O (holding every earlier stage under
+//      the old m) is then rescaled in TMEM once P V of the previous stage is
+//      done -- and goes on to the other group;
+//   3. P = 2^(x - m) as FP16 into shared memory for P V, and the group's
+//      running sum (kept under the reference the group last used and
+//      brought to the newer one whenever it changes).
+// The scores arrive in units of the kernel's score scale sl2 > 0 (its sign
+// was folded into Q), so a masked score of -inf gives P = 0 directly.
+// At the end of the unit both groups bring their sums to the final reference,
+// add them, and split the output columns (group wg writes 128 wg ... + 127).
 __device__ void softmax_unit(const GroupArgs& ga, Smem& sm, Cursor& cur, int r0, int Rg, int j,
-                             int nt, int nbw, int cap, int words_per_row)
+                             int nt, int nbw, int cap, int words_per_row, float sl2)
 {
     const PrefillArgs& a = ga.a;
-    const int t = threadIdx.x, half = t >> 7, slot = t & (kM - 1), wq = (t >> 5) & 3;
+    const int t = threadIdx.x, wg = t >> 7, slot = t & (kM - 1), wq = (t >> 5) & 3;
     const int rl = slot / a.G, h = slot - rl * a.G;
     const bool slot_ok = rl < Rg;
     const int own = slot_ok ? sm.row_own[rl] : -1;
     const int rank_own = slot_ok ? sm.row_rank_own[rl] : -1;
     const int tail_n = own >= 0 ? sm.row_p[rl] - 4 * own + 1 : 0;
+    const bool dup = own >= 0 && sm.row_dup[rl] != 0;
     const uint32_t tl = sm.tmem_base + ((uint32_t)(32 * wq) << 16);
-    const float sl2 = a.scale_log2;
-    float m_ref = -INFINITY, l = 0.f;
+    const int bar_in = (wg ? 2 : 6) + wq;      // the other group's reference arrives here
+    const int bar_out = (wg ? 6 : 2) + wq;     // this group's reference leaves here
+    float m_used = -INFINITY, l = 0.f;
     const uint32_t g0 = cur.g;
-    int ht0 = 0;
-    for (int i = 0; i < nt; ++i) {
+    int win = 0;                               // mask window of this group's latest stage
+    for (int i = wg; i < nt; i += 2) {
         const uint32_t g = g0 + i, buf = g & 1;
-        if (i - ht0 == cap) {
-            ht0 = i;
-            build_masks(ga, sm, r0, Rg, ht0, cap, words_per_row);
+        const int wi = i / cap;
+        while (win < wi) {                     // both groups rebuild every window once
+            ++win;
+            build_masks(ga, sm, r0, Rg, win * cap, cap, words_per_row);
         }
-        // live bits of this thread's 32 tokens (8 blocks of 4)
-        uint32_t live = 0u;
+        uint32_t live16 = 0u;                  // blocks of the stage the slot attends
         if (own >= 0) {
-            const int li = i - ht0;
-            uint32_t x8 =
-                (sm.masks[rl * words_per_row + (li >> 1)] >> (((li & 1) << 4) + 8 * half)) & 0xFFu;
-            // spread bit k to bit 4k, then fill each nibble
-            x8 = (x8 | (x8 << 12)) & 0x000F000Fu;
-            x8 = (x8 | (x8 << 6)) & 0x03030303u;
-            x8 = (x8 | (x8 << 3)) & 0x11111111u;
-            live = x8 * 0xFu;
-            if (rank_own >= 0 && (rank_own >> 4) == i) {
-                const int ko = (rank_own & 15) - 8 * half;
-                if (ko >= 0 && ko < 8)
-                    live &= ~((0xFu & ~((1u << tail_n) - 1u)) << (4 * ko));
-            }
+            const int li = i - wi * cap;
+            live16 = (sm.masks[rl * words_per_row + (li >> 1)] >> ((li & 1) << 4)) & 0xFFFFu;
         }
-        const bool dup = own >= 0 && sm.row_dup[rl] != 0;
 
         wait_or_abort(sm, &sm.s_full[buf], (g >> 1) & 1);
         tc::fence_after_sync();
-        uint32_t sv[32];
-        tc::tmem_ld32(tl + kTmemS + 64 * buf + 32 * half, sv);
+        uint32_t sv[64];
+        tc::tmem_ld32(tl + kTmemS + 64 * buf, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+        tc::tmem_ld32(tl + kTmemS + 64 * buf + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
         tc::tmem_wait_ld();
         tc::fence_before_sync();
-        tc::mbar_arrive(&sm.s_free[buf]);      // Q K^T of half-tile g + 2 may overwrite S
-        float x[32];
+        tc::mbar_arrive(&sm.s_free[buf]);      // Q K^T of stage g + 2 may overwrite S
+
+        float x[64];
 #pragma unroll
-        for (int c = 0; c < 32; ++c)
-            x[c] = ((live >> c) & 1u) ? __uint_as_float(sv[c]) * sl2 : -INFINITY;
+        for (int kb = 0; kb < kStageBlocks; ++kb) {
+            const bool pb = (live16 >> kb) & 1u;
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                x[4 * kb + u] = pb ? __uint_as_float(sv[4 * kb + u]) : -INFINITY;
+        }
+        if (rank_own >= 0 && (rank_own >> 4) == i) {   // the row's own block: tokens <= p
+            const int ko = rank_own & 15;
+#pragma unroll
+            for (int kb = 0; kb < kStageBlocks; ++kb)
+                if (kb == ko) {
+#pragma unroll
+                    for (int u = 1; u < 4; ++u)
+                        if (u >= tail_n)
+                            x[4 * kb + u] = -INFINITY;
+                }
+        }
         float mx[16];
 #pragma unroll
         for (int c = 0; c < 16; ++c)
-            mx[c] = fmaxf(x[c], x[c + 16]);
+            mx[c] = fmaxf(fmaxf(x[c], x[c + 16]), fmaxf(x[c + 32], x[c + 48]));
 #pragma unroll
         for (int w = 8; w >= 1; w >>= 1)
 #pragma unroll
             for (int c = 0; c < w; ++c)
                 mx[c] = fmaxf(mx[c], mx[c + w]);
-        // (double-buffered by stage parity: a half can only write the buffer
-        // again after both halves passed the next pair barrier)
-        sm.xm[i & 1][half][slot] = mx[0];
-        pair_sync(wq);
-        const float mt = fmaxf(mx[0], sm.xm[i & 1][half ^ 1][slot]);
+        const float mt = mx[0] * sl2;
 
-        bool resc = false;
-        float alpha = 1.f;
-        if (mt > m_ref + kRescaleSlack) {
-            alpha = ex2(m_ref - mt);             // 0 while nothing was attended yet
-            resc = m_ref != -INFINITY;
-            l *= alpha;
-            m_ref = mt;
+        // ---- the reference after this stage
+        float m_prev = -INFINITY;
+        if (i > 0) {
+            named_sync(bar_in);
+            m_prev = sm.mref[slot];
         }
-        if (__any_sync(0xffffffffu, resc)) {
-            // O still holds the sum under the old reference: wait for P V of
-            // the previous half-tile (P V before it on that buffer was waited
-            // for before P(g-1) was written; P V completes in issue order),
-            // then scale this thread's half of the lane's O row in place.
+        const float m_new = mt > m_prev + kRescaleSlack ? mt : m_prev;
+        sm.mref[slot] = m_new;
+        __threadfence_block();                 // the store is visible before the arrival
+        named_arrive(bar_out);
+        if (m_new != m_used) {                 // 0 while nothing was attended yet
+            l *= ex2(m_used - m_new);
+            m_used = m_new;
+        }
+        // ---- P(g) into shared-memory buffer buf once P V of stage g - 2 has
+        // consumed it: row = slot, 8 chunks of 8 tokens (128-byte swizzle)
+        if (g >= 2)
+            wait_or_abort(sm, &sm.p_free[buf], ((g >> 1) - 1) & 1);
+        // every column unconditionally (masked ones give 0): straight-line
+        // code lets the exponentials of all 64 columns overlap
+        const float m_off = m_new == -INFINITY ? 0.f : -m_new;
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+            const float p0 = ex2(fmaf(x[2 * c], sl2, m_off));
+            const float p1 = ex2(fmaf(x[2 * c + 1], sl2, m_off));
+            ls[c & 3] += p0 + p1;
+            pk[c] = pack_half2(p0, p1);
+        }
+        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        unsigned char* prow = sm.p[buf] + slot * 128;
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8)
+            *reinterpret_cast<uint4*>(prow + ((c8 ^ (slot & 7)) << 4)) =
+                make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
+        if (dup)                               // duplicated selections: count per listing
+            l += scale_listed(a, sm, prow, slot, r0 + rl, own, nbw, kStageBlocks * i, live16);
+        const bool resc = m_new != m_prev && m_prev != -INFINITY;
+        const bool any_resc = __any_sync(0xffffffffu, resc);
+        if (any_resc) {
+            // O holds stages < i under m_prev once P V of stage i - 1 is done
+            // (P V completes in issue order); scale the lane's O row in place
+            // before P(g) is published (P V of stage g adds to the scaled O).
             wait_or_abort(sm, &sm.p_free[(g - 1) & 1], ((g - 1) >> 1) & 1);
             tc::fence_after_sync();
-            const float f = resc ? alpha : 1.f;
+            const float f = resc ? ex2(m_prev - m_new) : 1.f;
 #pragma unroll 1
-            for (int c = 0; c < kD / 64; ++c) {
+            for (int c = 0; c < kD / 32; ++c) {
                 uint32_t o[32];
-                const uint32_t col = kTmemO + 128 * half + 32 * c;
+                const uint32_t col = kTmemO + 32 * c;
                 tc::tmem_ld32(tl + col, o);
                 tc::tmem_wait_ld();
 #pragma unroll
@@ -566,55 +693,30 @@ __device__ void softmax_unit(const GroupArgs& ga, Smem& sm, Cursor& cur, int r0,
             }
         }
 
-        uint32_t pk[16];
-        float lsum = 0.f;
-#pragma unroll
-        for (int kb = 0; kb < 8; ++kb) {
-            float pv[4] = {0.f, 0.f, 0.f, 0.f};
-            if (__any_sync(0xffffffffu, (live >> (4 * kb)) & 0xFu)) {
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    pv[u] = x[4 * kb + u] == -INFINITY ? 0.f : ex2(x[4 * kb + u] - m_ref);
-                if (dup && ((live >> (4 * kb)) & 0xFu)) {
-                    const int blk = kStageBlocks * i + 8 * half + kb;
-                    const float cnt =
-                        (float)listed_count(a, r0 + rl, block_of_rank(sm, nbw, blk), own);
-#pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        pv[u] *= cnt;
-                }
-            }
-            const __half2 p01 = __floats2half2_rn(pv[0], pv[1]);
-            const __half2 p23 = __floats2half2_rn(pv[2], pv[3]);
-            const float2 f01 = __half22float2(p01), f23 = __half22float2(p23);
-            lsum += (f01.x + f01.y) + (f23.x + f23.y);
-            pk[2 * kb] = *reinterpret_cast<const uint32_t*>(&p01);
-            pk[2 * kb + 1] = *reinterpret_cast<const uint32_t*>(&p23);
-        }
-        l += lsum;
-        // P(g) goes to shared-memory buffer buf once P V of half-tile g - 2
-        // has consumed it: row = slot, this half's 32 tokens = chunks
-        // 4 half .. 4 half + 3 of the 128-byte row (128-byte swizzle).
-        if (g >= 2)
-            wait_or_abort(sm, &sm.p_free[buf], ((g >> 1) - 1) & 1);
-        unsigned char* prow = sm.p[buf] + slot * 128;
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-            *reinterpret_cast<uint4*>(prow + (((4 * half + c) ^ (slot & 7)) << 4)) =
-                make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
         tc::fence_async_shared();
-        tc::tmem_wait_st();                    // O rescale stores, if any
+        if (any_resc)
+            tc::tmem_wait_st();                // the O rescale stores
         tc::fence_before_sync();
         tc::mbar_arrive(&sm.p_full[buf]);
     }
 
-    // Epilogue: O / l as binary16 (a row with nothing attended is zero), once
-    // the last P V is done (the one before it on that buffer was waited for
-    // before its P was written, so one parity wait is unambiguous).
-    sm.xl[half][slot] = l;
-    pair_sync(wq);
-    const float lt = l + sm.xl[half ^ 1][slot];
-    if (nt > 0) {
+    // ---- epilogue
+    const int last_win = nt > 0 ? (nt - 1) / cap : 0;
+    while (win < last_win) {                   // rebuilds the other group still makes
+        ++win;
+        build_masks(ga, sm, r0, Rg, win * cap, cap, words_per_row);
+    }
+    float m_fin = m_used;
+    if (nt > 0 && wg != ((nt - 1) & 1)) {      // the other group ran the last stage
+        named_sync(bar_in);
+        m_fin = sm.mref[slot];
+    }
+    if (m_fin != m_used)
+        l *= ex2(m_used - m_fin);
+    sm.xl[wg][slot] = l;
+    named_sync(10 + wq);
+    const float lt = l + sm.xl[wg ^ 1][slot];
+    if (nt > 0) {                              // the last P V is done
         const uint32_t g_last = g0 + nt - 1;
         wait_or_abort(sm, &sm.p_free[g_last & 1], (g_last >> 1) & 1);
         tc::fence_after_sync();
@@ -622,26 +724,25 @@ __device__ void softmax_unit(const GroupArgs& ga, Smem& sm, Cursor& cur, int r0,
     const float inv = lt > 0.f ? a.v_scale / lt : 0.f;     // E4M3: the per-tensor scale of V
     uint4* dst = slot_ok ? reinterpret_cast<uint4*>(
                                a.out + ((size_t)(r0 + rl) * a.Hq + (size_t)j * a.G + h) * kD +
-                               128 * half)
+                               128 * wg)
                          : nullptr;
 #pragma unroll 1
-    for (int c = 0; c < kD / 64; ++c) {
-        uint32_t o[32];
+    for (int c = 0; c < kD / 32; ++c) {
+        uint32_t o[16];
         if (nt > 0) {
-            tc::tmem_ld32(tl + kTmemO + 128 * half + 32 * c, o);
+            tc::tmem_ld16(tl + kTmemO + 128 * wg + 16 * c, o);
             tc::tmem_wait_ld();
         }
         if (dst != nullptr) {
-            uint32_t hv[16];
+            uint32_t hv[8];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
+            for (int e = 0; e < 8; ++e) {
                 const float v0 = (nt > 0 && lt > 0.f) ? __uint_as_float(o[2 * e]) * inv : 0.f;
                 const float v1 = (nt > 0 && lt > 0.f) ? __uint_as_float(o[2 * e + 1]) * inv : 0.f;
                 hv[e] = pack_half2(v0, v1);
             }
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                dst[4 * c + e] = make_uint4(hv[4 * e], hv[4 * e + 1], hv[4 * e + 2], hv[4 * e + 3]);
+            dst[2 * c] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+            dst[2 * c + 1] = make_uint4(hv[4], hv[5], hv[6], hv[7]);
         }
     }
     tc::fence_before_sync();
@@ -658,17 +759,19 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_prefill_grouped_kernel(con
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
     if (tid == 0) {
         for (int s = 0; s < kNS; ++s) {
-            tc::mbar_init(&sm.full[s], 32);
+            tc::mbar_init(&sm.full_k[s], 32);
+            tc::mbar_init(&sm.full_v[s], 32);
             tc::mbar_init(&sm.empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             tc::mbar_init(&sm.s_full[b], 1);
-            tc::mbar_init(&sm.s_free[b], kSoftWarps * 32);
-            tc::mbar_init(&sm.p_full[b], kSoftWarps * 32);
+            tc::mbar_init(&sm.s_free[b], kGroupThreads);   // one warpgroup reads S(g)
+            tc::mbar_init(&sm.p_full[b], kGroupThreads);   // and writes P(g)
             tc::mbar_init(&sm.p_free[b], 1);
         }
-        tc::mbar_init(&sm.done, 1);
+        tc::mbar_init(&sm.done, 2);                         // both MMA issuers commit
         sm.abort = 0;
+        sm.spin_limit = ga.spin_limit > 0 ? ga.spin_limit : tc::kSpinLimit;
         tc::mbar_init_fence();
     }
     if (w == kMmaWarp)
@@ -678,6 +781,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_prefill_grouped_kernel(con
     tc::fence_after_sync();
 
     Cursor cur;
+    SlotCount taken;                         // MMA threads: stages of their kind taken per slot
     const int C = gridDim.x;
     for (int wave = 0; wave * C < ga.n_units; ++wave) {
         const int u = wave * C + ((wave & 1) ? C - 1 - (int)blockIdx.x : (int)blockIdx.x);
@@ -688,21 +792,28 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_prefill_grouped_kernel(con
         const int words_per_row = kMaskWords / Rg, cap = 2 * words_per_row;
         unit_setup(ga, sm, r0, Rg, j, ga.nbw, words_per_row, cap);
         const int nt = (sm.n_union + kStageBlocks - 1) / kStageBlocks;
-        if (w >= kProdWarp0)
+        if (w >= kProdWarp0 && w < kProdWarp0 + kProdWarps)
             produce<kE4M3>(ga, sm, cur, j, ga.nbw, nt, sm.n_union);
         else if (w == kMmaWarp && lane == 0)
-            issue_mma(sm, cur, nt);
+            issue_qk(sm, cur, taken, nt);
+        else if (w == kPvWarp && lane == 0)
+            issue_pv(sm, cur, taken, nt);
         else if (w < kSoftWarps)
-            softmax_unit(ga, sm, cur, r0, Rg, j, nt, ga.nbw, cap, words_per_row);
+            softmax_unit(ga, sm, cur, r0, Rg, j, nt, ga.nbw, cap, words_per_row,
+                         a.scale_log2 == 0.f ? 1.f : fabsf(a.scale_log2));
         if (tid == 0 && sm.flags)
             raise_flag(a.err, sm.flags);
         tc::fence_before_sync();
         __syncthreads();
         tc::fence_after_sync();
     }
+    if ((w == kMmaWarp || w == kPvWarp) && lane == 0)
+        tc::mma_commit(&sm.done);            // arrives once this issuer's MMAs are done
     if (w == kMmaWarp && lane == 0) {        // every MMA done before TMEM is released
-        tc::mma_commit(&sm.done);
-        wait_or_abort(sm, &sm.done, 0);
+        // (waited for even after a time-out: the MMAs issued complete on
+        // their own, and TMEM must not be freed under them)
+        if (!tc::mbar_wait(&sm.done, 0, sm.spin_limit))
+            sm.abort = 1;
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -734,7 +845,7 @@ int grouped_prefill_rows(const PrefillArgs& a, int sms, int rows_per_group)
 }
 
 cudaError_t launch_prefill_grouped(const PrefillArgs& a, bool e4m3, int rows_per_group,
-                                   cudaStream_t s)
+                                   cudaStream_t s, long spin_limit, int stall_stage)
 {
     static std::atomic<int> attr_done[2][kMaxDevices];
     static std::atomic<int> sm_count[kMaxDevices];
@@ -769,6 +880,8 @@ cudaError_t launch_prefill_grouped(const PrefillArgs& a, bool e4m3, int rows_per
     ga.n_units = (int)(groups * a.Hkv);
     const int64_t blocks = a.kv_len > 0 ? ((int64_t)a.kv_len + 3) / 4 : 1;
     ga.nbw = (int)std::max<int64_t>(1, (blocks + 31) / 32);
+    ga.spin_limit = spin_limit;
+    ga.stall_stage = stall_stage;
     const int grid = std::min(ga.n_units, sms);
     if (e4m3)
         grp::sparse_prefill_grouped_kernel<true><<<grid, grp::kThreads, grp::kSmemBytes, s>>>(ga);

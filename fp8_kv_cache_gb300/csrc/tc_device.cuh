@@ -51,14 +51,14 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar)
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
-// Waits until the phase of parity `par` of *bar has completed; false when the
-// poll limit ran out first (about two seconds at most).  Each poll may
-// suspend the thread until the phase completes, so waiting warps leave their
-// issue slots to the warps that work.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t par)
+// Waits until the phase of parity `par` of *bar has completed; false when
+// `limit` polls ran out first (kSpinLimit polls: about two seconds at most).
+// Each poll may suspend the thread until the phase completes, so waiting
+// warps leave their issue slots to the warps that work.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t par, long limit = kSpinLimit)
 {
     const uint32_t a = smem_addr(bar);
-    for (long it = 0; it < kSpinLimit; ++it) {
+    for (long it = 0; it < limit; ++it) {
         uint32_t ok;
         asm volatile("{\n\t.reg .pred p;\n\t"
                      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
@@ -127,6 +127,17 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
                    "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
                    "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
                    "=r"(r[30]), "=r"(r[31])
+                 : "r"(taddr));
+}
+
+// 16 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16])
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+                 "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+                   "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
                  : "r"(taddr));
 }
 

@@ -160,14 +160,22 @@ int paged_gqa_decode(const void* q, const void* k_cache, const void* v_cache,
  *
  * Same arguments and results as paged_gqa_decode with the split route, except
  * that there is no workspace argument: the split scratch lives in a 16 MiB
- * static device array inside this library (held on every GPU that loads the
- * library until the process exits) and the call allocates nothing.  err_flag
- * is the optional device int of PAGED_GQA_FLAG_* bits.
- *  * Shapes whose scratch exceeds 16 MiB (paged_gqa_decode_workspace_size()
- *    above 16777216 bytes) are refused with PAGED_GQA_ERR_WORKSPACE before
- *    anything is launched.
+ * static device array inside this library (held on every GPU where the
+ * library's device code is loaded, until the process exits) and the call
+ * allocates nothing.  err_flag is the optional device int of
+ * PAGED_GQA_FLAG_* bits.
+ *  * Shapes whose split scratch for the given kv_dtype exceeds 16 MiB (the
+ *    workspace paged_gqa_decode would need with its automatic split count
+ *    for that dtype; never more than paged_gqa_decode_workspace_size()) are
+ *    refused with PAGED_GQA_ERR_WORKSPACE before anything is launched.
+ *    Batches above 4096 take the unsplit route and need no scratch.
  *  * The first call on each device looks up the array's device address with
- *    that device current; make that first call before any stream capture.
+ *    that device current.  Under the CUDA runtime's lazy module loading (its
+ *    default) that lookup loads the library's device code on that device,
+ *    which is when the 16 MiB is reserved: the first call can fail for lack
+ *    of memory and can synchronise.  Make one warm-up call per device at
+ *    initialisation, before any stream capture and outside any hook where
+ *    allocation is not allowed; later calls allocate nothing.
  *  * Every call shares the array: calls whose kernels may overlap on the GPU
  *    (e.g. on unordered streams) race and give wrong results; calls ordered
  *    on one stream are safe.  No scratch value needs to start at zero.
@@ -249,6 +257,30 @@ int paged_gqa_sparse_prefill_route(const void* q, const void* k_cache, const voi
                                    float kv_scale, float softmax_scale,
                                    void* out, int* err_flag, void* stream,
                                    int route, int rows_per_group);
+
+/*
+ * Test hook of the grouped route's failure path; the pages have no
+ * counterpart of it.  Runs paged_gqa_sparse_prefill_route with route =
+ * PAGED_GQA_PREFILL_GROUPED and rows_per_group = 0, except that every bounded
+ * wait of the kernel gives up after spin_limit polls (0 = the library's
+ * default of 2^20; at most 2^30) and, when stall_stage >= 0, that each CTA
+ * leaves its ring stage number stall_stage (counted from the CTA's start)
+ * unpublished, so the waits for it run out.  A CTA whose wait ran out skips
+ * its remaining waits, lets the tensor-core work it issued complete, frees
+ * its tensor memory and sets PAGED_GQA_FLAG_TIMEOUT in *err_flag; the output
+ * is then undefined.  No fault, trap or endless wait is involved, and later
+ * calls are unaffected.  Only tests of that path should call it.
+ * Returns PAGED_GQA_ERR_SHAPE for spin_limit outside [0, 2^30] or
+ * stall_stage < -1, else as paged_gqa_sparse_prefill_route.
+ */
+int paged_gqa_debug_grouped_prefill_stall(const void* q, const void* k_cache, const void* v_cache,
+                                          paged_gqa_kv_layout kv_layout, int kv_dtype,
+                                          const int32_t* block_table, int num_pages, int kv_len,
+                                          const int32_t* sel_idx, int n_sel, const int32_t* q_pos,
+                                          int R, int Hq, int Hkv, int D, int page_size,
+                                          float kv_scale, float softmax_scale, void* out,
+                                          int* err_flag, void* stream, long long spin_limit,
+                                          int stall_stage);
 
 /*
  * Rows per group of the grouped route for R query rows of Hq / Hkv heads on

@@ -3,8 +3,8 @@
 Every case compares the library's FP16 output element by element with the
 oracle's FP16-rounded output (max abs <= 2e-3, rel L2 <= 5e-4).  Full-size
 workloads run in the launch configuration the benchmark times (automatic
-split) and are checked on sampled (sequence, head) pairs the oracle computes
-one by one."""
+split) and are checked on every (sequence, head) row, with the strict 2e-3
+bound (no FP16-ULP allowance used)."""
 import numpy as np
 import pytest
 
@@ -58,7 +58,19 @@ def long_case():
     return c, U.dev_kv(c)
 
 
-def test_long_e4m3_sampled(long_case):
+def test_long_e4m3_every_row(long_case):
+    """The benchmark's long-context E4M3 workload: all 16 x 24 (sequence,
+    head) rows against the oracle."""
+    c, kv = long_case
+    got, flags = U.run_decode(c, kv=kv)
+    want, _, oflags = U.oracle_decode(c)
+    _, _, wide = U.assert_close(got, want, c.name)
+    assert wide == 0, f"{c.name}: {wide} elements needed the ULP allowance"
+    assert flags == oflags == 0
+
+
+def test_long_e4m3_sampled_pairs_match_full_oracle(long_case):
+    """The oracle's (sequence, head) pair mode agrees with its full mode."""
     c, kv = long_case
     _check_pairs(c, U.sample_pairs(c.B, c.Hq, per_seq=3, seed=1), kv=kv)
 
@@ -67,11 +79,8 @@ def test_long_e4m3_sampled(long_case):
 @pytest.mark.parametrize("L", [1024, 16384])
 @pytest.mark.parametrize("B", [1, 2, 4, 8, 16])
 def test_sweep(B, L, kvd):
-    c = W.sweep(B, L, kvd)
-    if L == 1024:
-        _check_full(c, strict=True)
-    else:
-        _check_pairs(c, U.sample_pairs(B, c.Hq, per_seq=2, seed=B))
+    """The batch/context grid ([D] Performance contract), every row."""
+    _check_full(W.sweep(B, L, kvd), strict=True)
 
 
 # ---------------------------------------------------------------- shapes and edges

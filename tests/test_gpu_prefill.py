@@ -146,37 +146,41 @@ def test_routes_agree_at_4096_rows_and_grouped_is_deterministic():
     assert np.array_equal(grouped.view(np.uint16), again.view(np.uint16)), "run-to-run"
 
 
-def test_full_4096_rows_sampled():
-    c = W.sparse_prefill_4096()
-    got, flags = U.run_prefill(c)
-    rows = np.random.default_rng(7).choice(c.R, size=24, replace=False).astype(np.int32)
-    rows = np.concatenate([rows, [0, c.R - 1]]).astype(np.int32)
-    want, _, oflags = U.oracle_prefill(c, rows=rows)
-    U.assert_close(got[rows], want[rows], c.name)
-    assert flags == 0 and oflags == 0
+def _every_row(c, routes):
+    """Every row of case c on each route against the oracle, strict bound."""
+    want, _, oflags = U.oracle_prefill(c)
+    outs = {}
+    for name, route in routes.items():
+        got, flags = U.run_prefill(c, **route)
+        _, _, wide = U.assert_close(got, want, f"{c.name} {name}")
+        assert wide == 0, f"{c.name} {name}: {wide} elements needed the ULP allowance"
+        assert flags == oflags, f"{c.name} {name}: flags {flags} != oracle {oflags}"
+        outs[name] = got
+    return outs
+
+
+ALL_ROUTES = {"auto": {}, "rowwise": dict(route=1), "grouped": dict(route=2)}
+
+
+@pytest.mark.parametrize("kvd", ["fp16", "e4m3"])
+def test_full_4096_rows_every_row_every_route(kvd):
+    """The 4096-row workload exactly as the benchmark times it ([P] Test
+    Result: the 4096-row interleaved-KV A/B), every row on the automatic,
+    per-row and grouped routes, FP16 and E4M3 caches; run to run bitwise."""
+    c = W.sparse_prefill_4096(kv_dtype=kvd)
+    outs = _every_row(c, ALL_ROUTES)
     again, _ = U.run_prefill(c)
-    assert np.array_equal(got.view(np.uint16), again.view(np.uint16)), "run-to-run"
+    assert np.array_equal(outs["auto"].view(np.uint16), again.view(np.uint16)), "run-to-run"
 
 
-def test_full_4096_rows_interleaved_e4m3_sampled():
-    """The E4M3 prefill exactly as the benchmark times it."""
-    c = W.sparse_prefill_4096(kv_dtype="e4m3")
-    got, flags = U.run_prefill(c)
-    rows = np.random.default_rng(9).choice(c.R, size=24, replace=False).astype(np.int32)
-    rows = np.concatenate([rows, [0, c.R - 1]]).astype(np.int32)
-    want, _, oflags = U.oracle_prefill(c, rows=rows)
-    U.assert_close(got[rows], want[rows], c.name)
-    assert flags == 0 and oflags == 0
-
-
-def test_full_4096_rows_e4m3_grouped_route_sampled():
-    c = W.sparse_prefill_4096(kv_dtype="e4m3")
-    got, flags = U.run_prefill(c, route=2)
-    rows = np.random.default_rng(11).choice(c.R, size=24, replace=False).astype(np.int32)
-    rows = np.concatenate([rows, [0, c.R - 1]]).astype(np.int32)
-    want, _, oflags = U.oracle_prefill(c, rows=rows)
-    U.assert_close(got[rows], want[rows], c.name + " grouped")
-    assert flags == 0 and oflags == 0
+@pytest.mark.parametrize("R", [1, 4095, 4097])
+def test_row_count_boundary(R):
+    """[P] Test Result: 4095 rows around the 4096-row route.  The grouped
+    route's rows per group depend on R (its groups fill whole waves), so
+    1, 4095 and 4097 rows take different partitions and ragged last groups;
+    4096 is the test above.  Every row on both routes."""
+    c = W.sparse_prefill_4096(R=R)
+    _every_row(c, {"rowwise": dict(route=1), "grouped": dict(route=2)})
 
 
 def test_full_4096_rows_contiguous_e4m3_sampled():
@@ -261,3 +265,38 @@ def test_grouped_route_head_groupings(Hq, Hkv, rows):
     sizes."""
     c = _small(230 + Hq + Hkv + rows, R=150, n_sel=256, first_block=2000, Hq=Hq, Hkv=Hkv)
     _check_full(c, dict(route=2, rows_per_group=rows))
+
+
+def test_grouped_wait_time_out_sets_the_flag_and_the_next_call_is_correct():
+    """The grouped kernel's bounded waits ([P] Changes: invalid requests are
+    inert, never fatal): through the test hook every wait gives up after
+    2000 polls (a few milliseconds) and each CTA leaves its fourth ring stage
+    unpublished, so the tensor-core thread's wait for it runs out.  The CTA
+    must skip its remaining waits, let its issued MMAs finish, free its
+    tensor memory and raise PAGED_GQA_FLAG_TIMEOUT; the context stays usable
+    and the next call is correct.  With no stall the hook is the normal
+    kernel."""
+    import torch
+    import fp8_kv_cache_gb300 as P
+    c = _small(240, R=37, n_sel=48, first_block=64)
+    _, k, v = U.dev_kv(c)
+    q, bt, sel, pos = U.dev(c.q), U.dev(c.block_table), U.dev(c.sel_idx), U.dev(c.q_pos)
+    want, _, _ = U.oracle_prefill(c)
+
+    def hook(spin_limit, stall_stage):
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        out = P.paged_gqa_debug_grouped_prefill_stall(
+            q, k, v, bt, c.kv_len, sel, pos, c.page_size, c.softmax_scale, c.kv_scale,
+            spin_limit=spin_limit, stall_stage=stall_stage, num_pages=c.num_pages, err_flag=err)
+        torch.cuda.synchronize()
+        return out.cpu().numpy(), int(err.item())
+
+    _, flags = hook(2000, 3)
+    assert flags & P.FLAG_TIMEOUT, flags
+    got, flags = hook(0, -1)                    # the hook without a stall
+    assert flags == 0
+    U.assert_close(got, want, "hook without a stall")
+    got = _check_full(c, dict(route=2))         # a normal call after the time-out
+    U.assert_close(got, want, "after the time-out")
+    with pytest.raises(P.PagedGQAError):
+        hook(-1, 0)
