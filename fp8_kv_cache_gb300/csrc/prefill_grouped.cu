@@ -84,6 +84,12 @@ struct Smem {
     float mref[kM];                          // [slot]: reference maximum handed between the groups
     float xl[2][kM];                         // [group][slot]: final sums exchanged
     uint64_t full_k[kNS], full_v[kNS], empty[kNS];   // K / V stage loaded, slot free
+    // Loaded stages of each kind taken so far from each ring slot, kept by
+    // the MMA thread that consumes that kind ([0]: K, [1]: V).  A slot's K
+    // and V occupants publish on separate barriers, so each consumer waits
+    // for every phase of its barriers in order: a parity wait is only
+    // unambiguous while its barrier is at most one phase behind.
+    uint32_t taken[2][kNS];
     uint64_t s_full[2], s_free[2], p_full[2], p_free[2], done;
     uint32_t tmem_base;
     int flags, n_union, abort;
@@ -99,14 +105,7 @@ struct Cursor {
     uint32_t g = 0;     // half-tile (S/P buffer) counter
 };
 
-// Loaded stages of one kind (K or V) taken so far from each ring slot, by the
-// MMA thread that consumes that kind.  A slot's K and V occupants publish on
-// separate barriers (full_k, full_v), so each consumer waits for every phase
-// of its barriers in order: a parity wait is only unambiguous while its
-// barrier is at most one phase behind the phase waited for.
-struct SlotCount {
-    uint32_t n[kNS] = {0u, 0u, 0u, 0u, 0u};
-};
+
 
 // Bounded wait; after any wait of the CTA has timed out, waits are skipped
 // (every role keeps its control flow, so all barriers are still reached and
@@ -313,13 +312,17 @@ __device__ void unit_setup(const GroupArgs& ga, Smem& sm, int r0, int Rg, int j,
     tc::fence_after_sync();
 }
 
-// Stage q of a unit with nt half-tiles.  The order is K0, K1, K2, V0, K3,
-// V1, ..., K(nt-1), V(nt-4), V(nt-3), V(nt-2), V(nt-1): Q K^T runs two
-// half-tiles ahead of P V, so the next scores are ready while the softmax of
-// the current half-tile and its P V run.
+// Stage q of a unit with nt half-tiles, in ring order: the K stages of the
+// first kKLead half-tiles, then V0, K(kKLead), V1, K(kKLead + 1), ..., and
+// the last V stages.  Q K^T of half-tile h runs once the softmax has read
+// the scores of h - 2 (two score buffers), so K stages loaded further ahead
+// only wait in the ring; leads of 2 to 5 half-tiles measured within 3 % of
+// each other on the 4096-row workload, 2 the fastest.
+constexpr int kKLead = 2;
+
 __device__ __forceinline__ void stage_of(int q, int nt, bool& is_v, int& ht)
 {
-    const int lead = nt < 3 ? nt : 3;
+    const int lead = nt < kKLead ? nt : kKLead;
     if (q < lead) {
         is_v = false;
         ht = q;
@@ -328,48 +331,70 @@ __device__ __forceinline__ void stage_of(int q, int nt, bool& is_v, int& ht)
     const int r = q - lead, pairs = 2 * (nt - lead);
     if (r < pairs) {
         is_v = (r & 1) == 0;
-        ht = is_v ? r >> 1 : (r >> 1) + 3;
+        ht = is_v ? r >> 1 : (r >> 1) + kKLead;
     } else {
         is_v = true;
         ht = r - pairs + (nt - lead);
     }
 }
 
+// Byte offset (K and V share it) of the first row of block lane (lanes
+// 0 .. 15) of the stage of half-tile ht, or -1 past the union or on other
+// lanes.
+__device__ __forceinline__ int64_t stage_block_offset(const GroupArgs& ga, const Smem& sm, int j,
+                                                      int nbw, int n_union, int ht, int lane)
+{
+    int64_t off = -1;
+    if (lane < kStageBlocks) {
+        const int k = kStageBlocks * ht + lane;
+        if (k < n_union) {
+            const int b = block_of_rank(sm, nbw, k);
+            int page, slot;
+            page_valid_block(ga.a.kv, ga.a.bt, b, page, slot);
+            off = row_offset(ga.a.kv, page, slot, j);
+        }
+    }
+    return off;
+}
+
 // Producer warps: warp pw owns ring slot pw and fills every stage that lands
-// there (stages it with it % kNS == pw): lanes 0..15 resolve the stage's 16
-// blocks (rank -> block -> page) in parallel.  FP16 rows: each lane copies its
-// 16-byte chunk of all 64 rows with cp.async and waits for its own copies.
-// E4M3 rows (256 codes): each lane loads 16-code chunks into registers,
-// converts them exactly to binary16 with the hardware converter and stores
-// the two 16-byte halves into the same tile layout.  The warp then fences its
-// writes for the tensor cores and publishes the stage; stages of different
-// warps are in flight together.
+// there (positions q with (it0 + q) % kNS == pw): lanes 0..15 resolve the
+// stage's 16 blocks (rank -> block -> page) in parallel, for the warp's next
+// stage while the current one's copies are in flight.  FP16 rows: each lane
+// copies its 16-byte chunk of all 64 rows with cp.async and waits for its
+// own copies.  E4M3 rows (256 codes): each lane loads 16-code chunks into
+// registers, converts them exactly to binary16 with the hardware converter
+// and stores the two 16-byte halves into the same tile layout.  The warp then
+// fences its writes for the tensor cores and publishes the stage on the
+// barrier of its kind; stages of different warps are in flight together.
 template <bool kE4M3>
 __device__ void produce(const GroupArgs& ga, Smem& sm, Cursor& cur, int j, int nbw, int nt,
                         int n_union)
 {
     const PrefillArgs& a = ga.a;
     const int lane = threadIdx.x & 31, pw = (threadIdx.x >> 5) - kProdWarp0;
-    for (int q = 0; q < 2 * nt; ++q, ++cur.it) {
-        const int s = cur.it % kNS;
-        if (s != pw)
-            continue;
-        bool is_v;
-        int ht;
+    const uint32_t it0 = cur.it;
+    const int n = 2 * nt;
+    int q = (pw - (int)(it0 % kNS) + kNS) % kNS;
+    bool is_v = false;
+    int ht = 0;
+    int64_t off = -1;
+    if (q < n) {
         stage_of(q, nt, is_v, ht);
-        if (cur.it >= (uint32_t)kNS)
-            wait_or_abort(sm, &sm.empty[s], ((cur.it / kNS) - 1) & 1);
-        int64_t off = -1;
-        if (lane < kStageBlocks) {
-            const int k = kStageBlocks * ht + lane;
-            if (k < n_union) {
-                const int b = block_of_rank(sm, nbw, k);
-                int page, slot;
-                page_valid_block(a.kv, a.bt, b, page, slot);
-                off = row_offset(a.kv, page, slot, j);
-            }
-        }
+        off = stage_block_offset(ga, sm, j, nbw, n_union, ht, lane);
+    }
+    for (; q < n; q += kNS) {
+        const uint32_t it = it0 + q;
+        const int s = pw;
+        if (it >= (uint32_t)kNS)
+            wait_or_abort(sm, &sm.empty[s], ((it / kNS) - 1) & 1);
         const unsigned char* base = is_v ? a.kv.v : a.kv.k;
+        const int qn = q + kNS;
+        bool nv = false;
+        int nh = 0;
+        if (qn < n)
+            stage_of(qn, nt, nv, nh);
+        int64_t off_next = -1;
         if (kE4M3) {
             // chunk idx = lane + 32 i: row idx / 16, codes 16 (idx % 16) .. + 15
             const uint32_t st = tc::smem_addr(sm.ring[s]);
@@ -399,6 +424,8 @@ __device__ void produce(const GroupArgs& ga, Smem& sm, Cursor& cur, int j, int n
                                  "r"(h[4]), "r"(h[5]), "r"(h[6]), "r"(h[7]) : "memory");
                 }
             }
+            if (qn < n)
+                off_next = stage_block_offset(ga, sm, j, nbw, n_union, nh, lane);
         } else {
             const uint32_t st = tc::smem_addr(sm.ring[s]) + (lane >> 3) * kRegionBytes;
             const uint32_t x = lane & 7;
@@ -416,12 +443,18 @@ __device__ void produce(const GroupArgs& ga, Smem& sm, Cursor& cur, int j, int n
                 }
             }
             cp_async_commit();
+            if (qn < n)                          // the next stage's rows, while these copies fly
+                off_next = stage_block_offset(ga, sm, j, nbw, n_union, nh, lane);
             cp_async_wait<0>();
         }
         tc::fence_async_shared();
-        if ((int)cur.it != ga.stall_stage)   // test hook: a stage left unpublished
+        if ((int)it != ga.stall_stage)       // test hook: a stage left unpublished
             tc::mbar_arrive(is_v ? &sm.full_v[s] : &sm.full_k[s]);
+        off = off_next;
+        is_v = nv;
+        ht = nh;
     }
+    cur.it = it0 + n;
 }
 
 // The two MMA issuer threads walk the unit's stages in ring order and each
@@ -430,7 +463,7 @@ __device__ void produce(const GroupArgs& ga, Smem& sm, Cursor& cur, int j, int n
 // stages back), independently of P V, which waits for the stage's
 // probabilities.  Both kinds share the tensor pipe; they touch disjoint TMEM
 // columns and shared-memory stages.
-__device__ void issue_qk(Smem& sm, Cursor& cur, SlotCount& taken, int nt)
+__device__ void issue_qk(Smem& sm, Cursor& cur, int nt)
 {
     constexpr uint32_t kIdQK = tc::f16_idesc(kM, kStageTokens, false, false);
     const uint32_t tm = sm.tmem_base;
@@ -443,7 +476,7 @@ __device__ void issue_qk(Smem& sm, Cursor& cur, SlotCount& taken, int nt)
             continue;
         const uint32_t g = g0 + ht, buf = g & 1, s = cur.it % kNS;
         const uint32_t st = tc::smem_addr(sm.ring[s]);
-        wait_or_abort(sm, &sm.full_k[s], taken.n[s]++ & 1);
+        wait_or_abort(sm, &sm.full_k[s], sm.taken[0][s]++ & 1);
         if (g >= 2)
             wait_or_abort(sm, &sm.s_free[buf], ((g >> 1) - 1) & 1);
         tc::fence_after_sync();
@@ -462,7 +495,7 @@ __device__ void issue_qk(Smem& sm, Cursor& cur, SlotCount& taken, int nt)
     cur.g = g0 + nt;
 }
 
-__device__ void issue_pv(Smem& sm, Cursor& cur, SlotCount& taken, int nt)
+__device__ void issue_pv(Smem& sm, Cursor& cur, int nt)
 {
     constexpr uint32_t kIdPV = tc::f16_idesc(kM, kD, false, true);
     const uint32_t tm = sm.tmem_base;
@@ -475,7 +508,7 @@ __device__ void issue_pv(Smem& sm, Cursor& cur, SlotCount& taken, int nt)
             continue;
         const uint32_t g = g0 + ht, buf = g & 1, s = cur.it % kNS;
         const uint32_t st = tc::smem_addr(sm.ring[s]);
-        wait_or_abort(sm, &sm.full_v[s], taken.n[s]++ & 1);
+        wait_or_abort(sm, &sm.full_v[s], sm.taken[1][s]++ & 1);
         wait_or_abort(sm, &sm.p_full[buf], (g >> 1) & 1);
         tc::fence_after_sync();
         const uint64_t da0 = tc::sw128_desc(tc::smem_addr(sm.p[buf]), 16, 1024);
@@ -770,6 +803,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_prefill_grouped_kernel(con
             tc::mbar_init(&sm.p_free[b], 1);
         }
         tc::mbar_init(&sm.done, 2);                         // both MMA issuers commit
+        for (int s = 0; s < kNS; ++s)
+            sm.taken[0][s] = sm.taken[1][s] = 0u;
         sm.abort = 0;
         sm.spin_limit = ga.spin_limit > 0 ? ga.spin_limit : tc::kSpinLimit;
         tc::mbar_init_fence();
@@ -781,7 +816,6 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_prefill_grouped_kernel(con
     tc::fence_after_sync();
 
     Cursor cur;
-    SlotCount taken;                         // MMA threads: stages of their kind taken per slot
     const int C = gridDim.x;
     for (int wave = 0; wave * C < ga.n_units; ++wave) {
         const int u = wave * C + ((wave & 1) ? C - 1 - (int)blockIdx.x : (int)blockIdx.x);
@@ -795,9 +829,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_prefill_grouped_kernel(con
         if (w >= kProdWarp0 && w < kProdWarp0 + kProdWarps)
             produce<kE4M3>(ga, sm, cur, j, ga.nbw, nt, sm.n_union);
         else if (w == kMmaWarp && lane == 0)
-            issue_qk(sm, cur, taken, nt);
+            issue_qk(sm, cur, nt);
         else if (w == kPvWarp && lane == 0)
-            issue_pv(sm, cur, taken, nt);
+            issue_pv(sm, cur, nt);
         else if (w < kSoftWarps)
             softmax_unit(ga, sm, cur, r0, Rg, j, nt, ga.nbw, cap, words_per_row,
                          a.scale_log2 == 0.f ? 1.f : fabsf(a.scale_log2));
