@@ -29,7 +29,8 @@ __all__ = [
     "paged_gqa_decode", "paged_gqa_decode_noalloc", "paged_gqa_sparse_prefill",
     "paged_gqa_sparse_prefill_route", "paged_gqa_sparse_prefill_group_rows", "PREFILL_AUTO",
     "PREFILL_ROWWISE", "PREFILL_GROUPED", "paged_gqa_debug_grouped_prefill_stall",
-    "paged_gqa_gather_dequant",
+    "paged_gqa_sparse_prefill_auto_route",
+    "paged_gqa_gather_dequant", "paged_gqa_sparse_gather_probe",
     "paged_gqa_sparse_prefill_tokens", "paged_gqa_decode_workspace_size",
     "paged_gqa_decode_workspace_size_splits",
     "paged_gqa_status_string", "paged_gqa_version", "Workspace",
@@ -111,6 +112,8 @@ def lib():
                 vp, vp, vp, KVLayout, i32, vp, i32, i32, vp, i32, vp, i32, i32, i32, i32, i32,
                 f32, f32, vp, vp, vp, ctypes.c_longlong, i32]
             L.paged_gqa_debug_grouped_prefill_stall.restype = i32
+            L.paged_gqa_sparse_prefill_auto_route.argtypes = [i32, i32, i32, i32, i32, i32]
+            L.paged_gqa_sparse_prefill_auto_route.restype = i32
             L.paged_gqa_sparse_prefill_group_rows.argtypes = [i32, i32, i32, i32]
             L.paged_gqa_sparse_prefill_group_rows.restype = i32
             L.paged_gqa_gather_dequant.argtypes = [vp, KVLayout, i32, vp, i64, vp, i32, i32, i32,
@@ -119,6 +122,9 @@ def lib():
             L.paged_gqa_sparse_prefill_tokens.argtypes = [vp, i32, i32, vp, i32, vp, i32, i32,
                                                           vp, vp]
             L.paged_gqa_sparse_prefill_tokens.restype = i32
+            L.paged_gqa_sparse_gather_probe.argtypes = [vp, vp, KVLayout, i32, vp, i32, i32, vp,
+                                                        i32, vp, i32, i32, i32, i32, vp, vp]
+            L.paged_gqa_sparse_gather_probe.restype = i32
             L.paged_gqa_select_blocks.argtypes = [vp, i64, i32, vp, i32, i32, i32, vp, vp, vp]
             L.paged_gqa_select_blocks.restype = i32
             L.paged_gqa_topk_topp_mask.argtypes = [vp, i64, vp, i64, i32, i32, i32, f32, vp, vp]
@@ -295,6 +301,14 @@ def paged_gqa_debug_grouped_prefill_stall(q, k_cache, v_cache, block_table, kv_l
     return out
 
 
+def paged_gqa_sparse_prefill_auto_route(R, Hq, Hkv, kv_len, n_sel, kv_dtype=KV_FP16) -> int:
+    """The route (PREFILL_ROWWISE or PREFILL_GROUPED) the automatic rule takes."""
+    n = lib().paged_gqa_sparse_prefill_auto_route(int(R), int(Hq), int(Hkv), int(kv_len),
+                                                  int(n_sel), int(kv_dtype))
+    _check(min(n, 0), "paged_gqa_sparse_prefill_auto_route")
+    return n
+
+
 def paged_gqa_sparse_prefill_group_rows(R, Hq, Hkv, rows_per_group=0) -> int:
     """Rows per group of the grouped prefill route on the current device."""
     n = lib().paged_gqa_sparse_prefill_group_rows(int(R), int(Hq), int(Hkv), int(rows_per_group))
@@ -348,6 +362,27 @@ def paged_gqa_sparse_prefill_tokens(block_table, num_pages, kv_len, sel_idx, q_p
         _ptr(block_table), num_pages, kv_len, _ptr(sel_idx) if n_sel else None, n_sel,
         _ptr(q_pos), R, page_size, _ptr(out), _stream(stream))
     _check(st, "paged_gqa_sparse_prefill_tokens")
+    return out
+
+
+def paged_gqa_sparse_gather_probe(k_cache, v_cache, block_table, kv_len, sel_idx, q_pos,
+                                  page_size, *, num_pages=None, out=None, stream=None):
+    """The per-row prefill route's gather alone (a measurement helper):
+    returns uint32 [R, Hkv], per row and KV head the XOR of every 32-bit word
+    of the K and V rows it attends."""
+    torch = _torch()
+    R = q_pos.shape[0]
+    Hkv, D = k_cache.shape[2], k_cache.shape[3]
+    n_sel = sel_idx.shape[1] if sel_idx.dim() == 2 else 0
+    if num_pages is None:
+        num_pages = k_cache.shape[0]
+    if out is None:
+        out = torch.empty((R, Hkv), dtype=torch.int32, device=k_cache.device)
+    st = lib().paged_gqa_sparse_gather_probe(
+        _ptr(k_cache), _ptr(v_cache), _layout(k_cache, v_cache), _kv_dtype(k_cache),
+        _ptr(block_table), num_pages, kv_len, _ptr(sel_idx) if n_sel else None, n_sel,
+        _ptr(q_pos), R, Hkv, D, page_size, _ptr(out), _stream(stream))
+    _check(st, "paged_gqa_sparse_gather_probe")
     return out
 
 

@@ -117,6 +117,20 @@ int prefill_route_impl(const void* q, const void* k_cache, const void* v_cache,
                        void* stream, int route, int rows_per_group, long spin_limit,
                        int stall_stage);
 
+// Automatic route choice (the grouped route must also support the shape):
+// the grouped kernel once rows select a large share of the sequence's blocks,
+// where the union of a row group is much smaller than the sum of its rows'
+// selections; below that the per-row kernel, which gathers at the L2
+// ceiling, is faster.  4096 rows over 32768 tokens cross over between 512
+// and 1024 selections with FP16 rows (32 n_sel >= kv_len) and between 1024
+// and 2048 with E4M3 rows, whose per-row gather moves half the bytes
+// (16 n_sel >= kv_len).
+bool auto_picks_grouped(int n_sel, int kv_len, bool e4m3)
+{
+    const int64_t density = e4m3 ? 16 : 32;
+    return density * n_sel >= (int64_t)kv_len;
+}
+
 }  // namespace
 
 extern "C" {
@@ -323,17 +337,9 @@ int prefill_route_impl(const void* q, const void* k_cache, const void* v_cache,
         return PAGED_GQA_ERR_UNSUPPORTED;
     if (rows_per_group > kGroupSlots / a.G)
         return PAGED_GQA_ERR_SHAPE;
-    // Automatic choice: the grouped kernel once rows select a large share of
-    // the sequence's blocks, where the union of a row group is much smaller
-    // than the sum of its rows' selections; below that the per-row kernel,
-    // which gathers at the L2 ceiling, is faster.  4096 rows over 32768
-    // tokens cross over between 512 and 1024 selections with FP16 rows
-    // (32 n_sel >= kv_len) and between 1024 and 2048 with E4M3 rows, whose
-    // per-row gather moves half the bytes (16 n_sel >= kv_len).
-    const int64_t density = e4m3 ? 16 : 32;
     const bool grouped = route == PAGED_GQA_PREFILL_GROUPED ||
                          (route == PAGED_GQA_PREFILL_AUTO && grouped_ok &&
-                          density * n_sel >= (int64_t)kv_len);
+                          auto_picks_grouped(n_sel, kv_len, e4m3));
     const cudaError_t e =
         grouped ? launch_prefill_grouped(a, e4m3, rows_per_group, static_cast<cudaStream_t>(stream),
                                          spin_limit, stall_stage)
@@ -344,6 +350,25 @@ int prefill_route_impl(const void* q, const void* k_cache, const void* v_cache,
 }  // namespace
 
 extern "C" {
+
+int paged_gqa_sparse_prefill_auto_route(int R, int Hq, int Hkv, int kv_len, int n_sel,
+                                        int kv_dtype)
+{
+    if (R < 0 || n_sel < 0 || Hq < 1 || Hkv < 1 || kv_len < 0 || Hq % Hkv != 0)
+        return PAGED_GQA_ERR_SHAPE;
+    if (Hq / Hkv > kGMax || (kv_dtype != PAGED_GQA_KV_FP16 && kv_dtype != PAGED_GQA_KV_E4M3))
+        return PAGED_GQA_ERR_UNSUPPORTED;
+    PrefillArgs a{};
+    a.R = R;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.G = Hq / Hkv;
+    a.kv_len = kv_len;
+    return grouped_prefill_supported(a) && auto_picks_grouped(n_sel, kv_len,
+                                                               kv_dtype == PAGED_GQA_KV_E4M3)
+               ? PAGED_GQA_PREFILL_GROUPED
+               : PAGED_GQA_PREFILL_ROWWISE;
+}
 
 int paged_gqa_sparse_prefill_group_rows(int R, int Hq, int Hkv, int rows_per_group)
 {
@@ -390,6 +415,43 @@ int paged_gqa_gather_dequant(const void* cache, paged_gqa_kv_layout kv_layout, i
     const cudaError_t e = launch_gather(g, kv_dtype == PAGED_GQA_KV_E4M3, block_table,
                                        bt_row_stride, seq_lens, B, T, Hkv, max_seq_len, kv_scale,
                                        out, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PAGED_GQA_OK : PAGED_GQA_ERR_CUDA;
+}
+
+int paged_gqa_sparse_gather_probe(const void* k_cache, const void* v_cache,
+                                  paged_gqa_kv_layout kv_layout, int kv_dtype,
+                                  const int32_t* block_table, int num_pages, int kv_len,
+                                  const int32_t* sel_idx, int n_sel, const int32_t* q_pos, int R,
+                                  int Hkv, int D, int page_size, uint32_t* out, void* stream)
+{
+    if (R < 0 || n_sel < 0 || kv_len < 0 || Hkv < 1 || Hkv > 65535 || num_pages < 1 ||
+        page_size < 4 || page_size % 4 != 0 || n_sel > (1 << 28))
+        return PAGED_GQA_ERR_SHAPE;
+    if (D != kD)
+        return PAGED_GQA_ERR_UNSUPPORTED;
+    int st = check_kv(k_cache, v_cache, kv_layout, kv_dtype);
+    if (st != PAGED_GQA_OK)
+        return st;
+    if (block_table == nullptr || q_pos == nullptr || out == nullptr ||
+        (n_sel > 0 && sel_idx == nullptr))
+        return PAGED_GQA_ERR_NULL_POINTER;
+    if ((reinterpret_cast<uintptr_t>(out) & 3u) != 0)
+        return PAGED_GQA_ERR_ALIGNMENT;
+    if (R == 0)
+        return PAGED_GQA_OK;
+    PrefillArgs a{};
+    a.kv = make_geom(k_cache, v_cache, kv_layout, kv_dtype, page_size, num_pages);
+    a.bt = block_table;
+    a.kv_len = kv_len;
+    a.sel = sel_idx;
+    a.n_sel = n_sel;
+    a.q_pos = q_pos;
+    a.R = R;
+    a.Hkv = Hkv;
+    a.Hq = Hkv;
+    a.G = 1;
+    const cudaError_t e = launch_sparse_gather(a, kv_dtype == PAGED_GQA_KV_E4M3, out,
+                                               static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PAGED_GQA_OK : PAGED_GQA_ERR_CUDA;
 }
 

@@ -110,6 +110,7 @@ int mask_slice(int V);
 bool mask_supported(int V, int k);
 cudaError_t launch_topk_topp(const MaskArgs& a, cudaStream_t s);
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t s);
+cudaError_t launch_sparse_gather(const PrefillArgs& a, bool e4m3, uint32_t* out, cudaStream_t s);
 cudaError_t launch_prefill_tokens(const KVGeom& g, const int32_t* bt, int kv_len,
                                   const int32_t* sel, int n_sel, const int32_t* q_pos, int R,
                                   int32_t* out, cudaStream_t s);

@@ -259,6 +259,17 @@ int paged_gqa_sparse_prefill_route(const void* q, const void* k_cache, const voi
                                    int route, int rows_per_group);
 
 /*
+ * The kernel route PAGED_GQA_PREFILL_AUTO takes for this shape:
+ * PAGED_GQA_PREFILL_ROWWISE or PAGED_GQA_PREFILL_GROUPED (the rule above,
+ * for kv_dtype PAGED_GQA_KV_FP16 or PAGED_GQA_KV_E4M3), or a negative
+ * status for invalid arguments.  Host only; launches nothing.  The pages
+ * have no counterpart of this helper: it tells a caller which design its
+ * calls run (for benchmarks and reports).
+ */
+int paged_gqa_sparse_prefill_auto_route(int R, int Hq, int Hkv, int kv_len, int n_sel,
+                                        int kv_dtype);
+
+/*
  * Test hook of the grouped route's failure path; the pages have no
  * counterpart of it.  Runs paged_gqa_sparse_prefill_route with route =
  * PAGED_GQA_PREFILL_GROUPED and rows_per_group = 0, except that every bounded
@@ -378,6 +389,26 @@ int paged_gqa_gather_dequant(const void* cache, paged_gqa_kv_layout kv_layout, i
 int paged_gqa_sparse_prefill_tokens(const int32_t* block_table, int num_pages, int kv_len,
                                     const int32_t* sel_idx, int n_sel, const int32_t* q_pos,
                                     int R, int page_size, int32_t* out, void* stream);
+
+/*
+ * Measurement helper; the pages have no counterpart of it.  Runs the gather
+ * of the per-row sparse-prefill kernel (PAGED_GQA_PREFILL_ROWWISE) alone:
+ * every row's selected four-token blocks and causal tail, K and V rows,
+ * copied through the same shared-memory rings with the same launch shape,
+ * entry table and inert rules, and each copied row read once from shared
+ * memory, with no attention arithmetic.  Its time is the ceiling of that
+ * gather on the device, the bound the per-row route is measured against.
+ *  arguments    as for paged_gqa_sparse_prefill (no q, no softmax scales).
+ *  out          device uint32 [R, Hkv]: the XOR of every 32-bit word of the
+ *               K and V rows row r attends through KV head j (0 for a row
+ *               that attends nothing), so tests can check the gather exactly.
+ * One kernel is launched; nothing is allocated.
+ */
+int paged_gqa_sparse_gather_probe(const void* k_cache, const void* v_cache,
+                                  paged_gqa_kv_layout kv_layout, int kv_dtype,
+                                  const int32_t* block_table, int num_pages, int kv_len,
+                                  const int32_t* sel_idx, int n_sel, const int32_t* q_pos, int R,
+                                  int Hkv, int D, int page_size, uint32_t* out, void* stream);
 
 /* Human-readable name of a status code (static string). */
 const char* paged_gqa_status_string(int status);

@@ -83,3 +83,41 @@ def test_prefill_token_lists(case):
         want = oracle.sparse_row_tokens(c.block_table, c.num_pages, c.kv_len, c.sel_idx[r],
                                         c.q_pos[r], c.page_size)
         assert np.array_equal(got, want), f"row {r}"
+
+
+def _xor_words(rows):
+    """XOR of every 32-bit word of the given rows (any shape, whole rows)."""
+    a = np.ascontiguousarray(rows).reshape(-1).view(np.uint32)
+    return int(np.bitwise_xor.reduce(a)) if a.size else 0
+
+
+@pytest.mark.parametrize("kvd", ["fp16", "e4m3"])
+@pytest.mark.parametrize("case", ["small", "full"])
+def test_sparse_gather_probe_reads_exactly_the_attended_rows(case, kvd):
+    """The gather-ceiling probe folds every word of the K and V rows each
+    row attends (selected blocks, causal tail, inert entries skipped), so its
+    per-row XOR equals the XOR of those rows read from the host copy."""
+    if case == "full":
+        c = W.sparse_prefill_4096(kv_dtype=kvd)
+        rows = np.random.default_rng(4).choice(c.R, size=40, replace=False)
+    else:
+        c = W.prefill_case(f"gprobe_{kvd}", R=40, n_sel=30, seed=203, first_block=40,
+                           tails=(1, 2, 3, 4), kv_dtype=kvd, Hq=12, Hkv=2)
+        c.sel_idx[3, 2] = -1
+        c.sel_idx[4, 0] = c.q_pos[4] // 4
+        c.q_pos[5] = -1
+        c.q_pos[6] = c.kv_len + 3
+        c.block_table[1] = -1
+        rows = np.arange(c.R)
+    _, k, v = U.dev_kv(c)
+    got = P.paged_gqa_sparse_gather_probe(k, v, U.dev(c.block_table), c.kv_len, U.dev(c.sel_idx),
+                                          U.dev(c.q_pos), c.page_size,
+                                          num_pages=c.num_pages).cpu().numpy().view(np.uint32)
+    for r in rows:
+        toks = oracle.sparse_row_tokens(c.block_table, c.num_pages, c.kv_len, c.sel_idx[r],
+                                        c.q_pos[r], c.page_size)
+        pages = c.block_table[toks // c.page_size]
+        slots = toks % c.page_size
+        for j in range(c.Hkv):
+            want = _xor_words(c.k[pages, slots, j]) ^ _xor_words(c.v[pages, slots, j])
+            assert int(got[r, j]) == want, f"row {r} head {j}"
