@@ -64,8 +64,9 @@ constexpr int kRegionBytes = kStageTokens * 128;      // 64 head-dim columns of 
 constexpr int kStageBytes = kStageTokens * kD * 2;    // 32 KB
 constexpr int kMaskWords = 4096;             // 16 KB of per-row stage masks
 constexpr int kSoftWarps = 8, kMmaWarp = 8, kProdWarps = kNS, kProdWarp0 = 9;
-constexpr int kPvWarp = kProdWarp0 + kProdWarps;   // issues P V; kMmaWarp issues Q K^T
-constexpr int kThreads = 32 * (kSoftWarps + 1 + kProdWarps + 1);
+constexpr int kPvWarp = kProdWarp0 + kProdWarps;   // issues P V
+constexpr int kQkWarp1 = kPvWarp + 1;               // with kMmaWarp: Q K^T of odd / even stages
+constexpr int kThreads = 32 * (kSoftWarps + 1 + kProdWarps + 2);
 constexpr int kGroupThreads = kSoftWarps / 2 * 32;   // one softmax warpgroup
 constexpr float kRescaleSlack = 8.f;         // log2-domain growth tolerated before rescaling O
 constexpr uint32_t kTmemCols = 512;
@@ -83,13 +84,15 @@ struct Smem {
     int row_p[kM], row_own[kM], row_rank_own[kM], row_dup[kM];
     float mref[kM];                          // [slot]: reference maximum handed between the groups
     float xl[2][kM];                         // [group][slot]: final sums exchanged
-    uint64_t full_k[kNS], full_v[kNS], empty[kNS];   // K / V stage loaded, slot free
-    // Loaded stages of each kind taken so far from each ring slot, kept by
-    // the MMA thread that consumes that kind ([0]: K, [1]: V).  A slot's K
-    // and V occupants publish on separate barriers, so each consumer waits
-    // for every phase of its barriers in order: a parity wait is only
-    // unambiguous while its barrier is at most one phase behind.
-    uint32_t taken[2][kNS];
+    // K stage loaded (by the parity of its half-tile in the unit), V stage
+    // loaded, slot free.
+    uint64_t full_k[2][kNS], full_v[kNS], empty[kNS];
+    // Stages taken so far from each ring slot by each MMA thread ([0], [1]:
+    // the Q K^T threads of even and odd half-tiles, [2]: P V).  Each kind of
+    // stage publishes on its own barrier, so every consumer waits for every
+    // phase of its barriers in order: a parity wait is only unambiguous
+    // while its barrier is at most one phase behind.
+    uint32_t taken[3][kNS];
     uint64_t s_full[2], s_free[2], p_full[2], p_free[2], done;
     uint32_t tmem_base;
     int flags, n_union, abort;
@@ -449,7 +452,7 @@ __device__ void produce(const GroupArgs& ga, Smem& sm, Cursor& cur, int j, int n
         }
         tc::fence_async_shared();
         if ((int)it != ga.stall_stage)       // test hook: a stage left unpublished
-            tc::mbar_arrive(is_v ? &sm.full_v[s] : &sm.full_k[s]);
+            tc::mbar_arrive(is_v ? &sm.full_v[s] : &sm.full_k[ht & 1][s]);
         off = off_next;
         is_v = nv;
         ht = nh;
@@ -463,7 +466,7 @@ __device__ void produce(const GroupArgs& ga, Smem& sm, Cursor& cur, int j, int n
 // stages back), independently of P V, which waits for the stage's
 // probabilities.  Both kinds share the tensor pipe; they touch disjoint TMEM
 // columns and shared-memory stages.
-__device__ void issue_qk(Smem& sm, Cursor& cur, int nt)
+__device__ void issue_qk(Smem& sm, Cursor& cur, int nt, int par)
 {
     constexpr uint32_t kIdQK = tc::f16_idesc(kM, kStageTokens, false, false);
     const uint32_t tm = sm.tmem_base;
@@ -472,11 +475,11 @@ __device__ void issue_qk(Smem& sm, Cursor& cur, int nt)
         bool is_v;
         int ht;
         stage_of(q, nt, is_v, ht);
-        if (is_v)
+        if (is_v || (ht & 1) != par)
             continue;
         const uint32_t g = g0 + ht, buf = g & 1, s = cur.it % kNS;
         const uint32_t st = tc::smem_addr(sm.ring[s]);
-        wait_or_abort(sm, &sm.full_k[s], sm.taken[0][s]++ & 1);
+        wait_or_abort(sm, &sm.full_k[par][s], sm.taken[par][s]++ & 1);
         if (g >= 2)
             wait_or_abort(sm, &sm.s_free[buf], ((g >> 1) - 1) & 1);
         tc::fence_after_sync();
@@ -508,7 +511,7 @@ __device__ void issue_pv(Smem& sm, Cursor& cur, int nt)
             continue;
         const uint32_t g = g0 + ht, buf = g & 1, s = cur.it % kNS;
         const uint32_t st = tc::smem_addr(sm.ring[s]);
-        wait_or_abort(sm, &sm.full_v[s], sm.taken[1][s]++ & 1);
+        wait_or_abort(sm, &sm.full_v[s], sm.taken[2][s]++ & 1);
         wait_or_abort(sm, &sm.p_full[buf], (g >> 1) & 1);
         tc::fence_after_sync();
         const uint64_t da0 = tc::sw128_desc(tc::smem_addr(sm.p[buf]), 16, 1024);
@@ -792,7 +795,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_prefill_grouped_kernel(con
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
     if (tid == 0) {
         for (int s = 0; s < kNS; ++s) {
-            tc::mbar_init(&sm.full_k[s], 32);
+            tc::mbar_init(&sm.full_k[0][s], 32);
+            tc::mbar_init(&sm.full_k[1][s], 32);
             tc::mbar_init(&sm.full_v[s], 32);
             tc::mbar_init(&sm.empty[s], 1);
         }
@@ -802,9 +806,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_prefill_grouped_kernel(con
             tc::mbar_init(&sm.p_full[b], kGroupThreads);   // and writes P(g)
             tc::mbar_init(&sm.p_free[b], 1);
         }
-        tc::mbar_init(&sm.done, 2);                         // both MMA issuers commit
+        tc::mbar_init(&sm.done, 3);                         // all three MMA issuers commit
         for (int s = 0; s < kNS; ++s)
-            sm.taken[0][s] = sm.taken[1][s] = 0u;
+            sm.taken[0][s] = sm.taken[1][s] = sm.taken[2][s] = 0u;
         sm.abort = 0;
         sm.spin_limit = ga.spin_limit > 0 ? ga.spin_limit : tc::kSpinLimit;
         tc::mbar_init_fence();
@@ -829,7 +833,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_prefill_grouped_kernel(con
         if (w >= kProdWarp0 && w < kProdWarp0 + kProdWarps)
             produce<kE4M3>(ga, sm, cur, j, ga.nbw, nt, sm.n_union);
         else if (w == kMmaWarp && lane == 0)
-            issue_qk(sm, cur, nt);
+            issue_qk(sm, cur, nt, 0);
+        else if (w == kQkWarp1 && lane == 0)
+            issue_qk(sm, cur, nt, 1);
         else if (w == kPvWarp && lane == 0)
             issue_pv(sm, cur, nt);
         else if (w < kSoftWarps)
@@ -841,7 +847,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_prefill_grouped_kernel(con
         __syncthreads();
         tc::fence_after_sync();
     }
-    if ((w == kMmaWarp || w == kPvWarp) && lane == 0)
+    if ((w == kMmaWarp || w == kPvWarp || w == kQkWarp1) && lane == 0)
         tc::mma_commit(&sm.done);            // arrives once this issuer's MMAs are done
     if (w == kMmaWarp && lane == 0) {        // every MMA done before TMEM is released
         // (waited for even after a time-out: the MMAs issued complete on
