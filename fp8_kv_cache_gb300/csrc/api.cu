@@ -118,16 +118,17 @@ int prefill_route_impl(const void* q, const void* k_cache, const void* v_cache,
                        int stall_stage);
 
 // Automatic route choice (the grouped route must also support the shape):
-// the grouped kernel once rows select a large share of the sequence's blocks,
-// where the union of a row group is much smaller than the sum of its rows'
-// selections; below that the per-row kernel, which gathers at the L2
-// ceiling, is faster.  4096 rows over 32768 tokens cross over between 512
-// and 1024 selections with FP16 rows (32 n_sel >= kv_len) and between 1024
-// and 2048 with E4M3 rows, whose per-row gather moves half the bytes
-// (16 n_sel >= kv_len).
+// the grouped kernel once rows select enough of the sequence's blocks that
+// the union of a row group is much smaller than the sum of its rows'
+// selections; below that the per-row kernel is faster.  Measured on 4096
+// rows over 32768 tokens: FP16 rows cross over at about 384 selections
+// (0.61 ms both), grouped 0.72 vs 0.79 ms at 512 and 1.13 vs 2.89 ms at
+// 2048 (64 n_sel >= kv_len); E4M3 rows, whose per-row gather moves half the
+// bytes while the grouped route converts them to binary16 as it gathers,
+// cross over at about 1536 (16 n_sel >= kv_len).
 bool auto_picks_grouped(int n_sel, int kv_len, bool e4m3)
 {
-    const int64_t density = e4m3 ? 16 : 32;
+    const int64_t density = e4m3 ? 16 : 64;
     return density * n_sel >= (int64_t)kv_len;
 }
 

@@ -248,3 +248,52 @@ def test_binding_fails_loudly_without_library(monkeypatch):
     monkeypatch.setattr(P, "library_path", "/nonexistent/libpaged_gqa.so")
     with pytest.raises(RuntimeError, match="no fallback"):
         P.lib()
+
+
+def test_auto_route_follows_the_documented_rule(L):
+    """PAGED_GQA_PREFILL_AUTO: grouped when 64 n_sel >= kv_len (FP16) or
+    16 n_sel >= kv_len (E4M3), and the grouped route supports the shape."""
+    f = L.paged_gqa_sparse_prefill_auto_route
+    assert f(4096, 6, 1, 32768, 512, 0) == 2           # FP16, 64 * 512 = 32768
+    assert f(4096, 6, 1, 32768, 511, 0) == 1
+    assert f(4096, 6, 1, 32768, 2048, 1) == 2          # E4M3, 16 * 2048 = 32768
+    assert f(4096, 6, 1, 32768, 2047, 1) == 1
+    assert f(4096, 6, 1, 131076, 4096, 0) == 1         # beyond the grouped route's bitmap
+    assert f(-1, 6, 1, 32768, 512, 0) == -3
+    assert f(10, 7, 2, 32768, 512, 0) == -3
+    assert f(10, 12, 1, 32768, 512, 0) == -4           # 12 query heads per KV head
+    assert f(10, 6, 1, 32768, 512, 5) == -4            # unknown KV dtype
+
+
+@host_only
+def test_gather_probe_and_stall_hook_validate(L):
+    lay = P.KVLayout(16 * 512, 512, 256)
+    # (k, v, layout, dtype, bt, num_pages, kv_len, sel, n_sel, q_pos, R, Hkv, D, page, out, stream)
+    ok = [A, A, lay, 0, A, 2048, 32768, A, 512, A, 4096, 1, 256, 16, A, None]
+
+    def probe(**kw):
+        a = list(ok)
+        names = ["k", "v", "lay", "dtype", "bt", "num_pages", "kv_len", "sel", "n_sel", "qp", "R",
+                 "Hkv", "D", "P", "out", "stream"]
+        for k_, v_ in kw.items():
+            a[names.index(k_)] = v_
+        return L.paged_gqa_sparse_gather_probe(*a)
+
+    assert probe(k=None) == -1 and probe(out=None) == -1 and probe(sel=None) == -1
+    assert probe(out=A + 2) == -2 and probe(k=A + 8) == -2
+    assert probe(R=-1) == -3 and probe(P=6) == -3 and probe(Hkv=0) == -3
+    assert probe(D=128) == -4 and probe(dtype=3) == -4
+    assert probe(R=0) == 0
+    # the stall hook: its own limits, then the route's validation
+    args = [A, A, A, lay, 0, A, 2048, 32768, A, 512, A, 4096, 6, 1, 256, 16, 1.0, 0.0625, A,
+            None, None]
+    stall = L.paged_gqa_debug_grouped_prefill_stall
+    assert stall(*args, -1, 0) == -3
+    assert stall(*args, (1 << 30) + 1, 0) == -3
+    assert stall(*args, 1000, -2) == -3
+    bad_q = list(args)
+    bad_q[0] = None
+    assert stall(*bad_q, 1000, 3) == -1
+    zero_r = list(args)
+    zero_r[11] = 0
+    assert stall(*zero_r, 1000, 3) == 0
