@@ -71,13 +71,14 @@ __device__ __forceinline__ int64_t effective_ctas(const DecodeArgs& a, int64_t T
 // (16-token tiles, round-robin), then merged into out_rows (final) or slot
 // (partial).  CTA-uniform: every thread of the CTA calls it.
 template <bool kE4M3>
-__device__ void run_piece(const DecodeArgs& a, const CtaSmem<kE4M3>& cs,
+__device__ void run_piece(const DecodeArgs& a, const CtaSmem<kE4M3, kDecodeWarps<kE4M3>()>& cs,
                           WarpRing<kE4M3, kStages<kE4M3>()>& rg, int b, int j, int L, int ta,
                           int te, __half* out_rows, float* slot, int& flags)
 {
+    constexpr int NW = kDecodeWarps<kE4M3>();
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     using Core = WarpCore<kE4M3>;
-    Core::stage_q(cs.qs, a.q + ((size_t)b * a.Hq + (size_t)j * a.G) * kD, a.G, lane, w);
+    Core::stage_q(cs.qs, a.q + ((size_t)b * a.Hq + (size_t)j * a.G) * kD, a.G, lane, w, NW);
     __syncthreads();
     Core wc;
     wc.reset();
@@ -93,9 +94,9 @@ __device__ void run_piece(const DecodeArgs& a, const CtaSmem<kE4M3>& cs,
         }
         return -1;
     };
-    run_tiles<kE4M3, kStages<kE4M3>()>(wc, rg, cs.qs, a.kv.k, a.kv.v, ta + w, te, kWarps, a.G,
+    run_tiles<kE4M3, kStages<kE4M3>()>(wc, rg, cs.qs, a.kv.k, a.kv.v, ta + w, te, NW, a.G,
                                        a.scale_log2, lane, offset);
-    cta_merge<kE4M3>(*cs.merge, wc, a.G, a.v_scale, out_rows, slot);
+    cta_merge<kE4M3, false, NW>(*cs.merge, wc, a.G, a.v_scale, out_rows, slot);
 }
 
 __device__ void zero_rows(__half* rows, int G)
@@ -107,10 +108,12 @@ __device__ void zero_rows(__half* rows, int G)
 }  // namespace
 
 template <bool kE4M3>
-__global__ void __launch_bounds__(kThreads, kMinCtas<kE4M3>()) decode_split_kernel(DecodeArgs a)
+__global__ void __launch_bounds__(32 * kDecodeWarps<kE4M3>(), kMinCtas<kE4M3>())
+    decode_split_kernel(DecodeArgs a)
 {
+    constexpr int NW = kDecodeWarps<kE4M3>(), NT = 32 * NW;
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    const CtaSmem<kE4M3> cs = CtaSmem<kE4M3>::carve(smem_raw, threadIdx.x >> 5);
+    const CtaSmem<kE4M3, NW> cs = CtaSmem<kE4M3, NW>::carve(smem_raw, threadIdx.x >> 5);
     WarpRing<kE4M3, kStages<kE4M3>()> rg;
     rg.init(cs.ring, cs.masks);
     int flags = 0;
@@ -142,7 +145,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas<kE4M3>()) decode_split_kern
     int64_t* P = reinterpret_cast<int64_t*>(cs.tail);
     int64_t* wtot = P + (a.B + 1);
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-    const int per = (a.B + kThreads - 1) / kThreads;
+    const int per = (a.B + NT - 1) / NT;
     const int b0 = min(a.B, tid * per), b1 = min(a.B, b0 + per);
     int64_t local = 0;
     for (int b = b0; b < b1; ++b) {
@@ -162,7 +165,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas<kE4M3>()) decode_split_kern
     if (lane == 31) wtot[w] = incl;
     __syncthreads();
     int64_t base = 0, total = 0;
-    for (int i = 0; i < kWarps; ++i) {
+    for (int i = 0; i < NW; ++i) {
         if (i < w) base += wtot[i];
         total += wtot[i];
     }
@@ -177,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas<kE4M3>()) decode_split_kern
     const int64_t T = (int64_t)a.Hkv * total;
     const int64_t C = T > 0 ? effective_ctas(a, T) : 0;
     if (blockIdx.x == 0 && a.B > kMergeScanMax) {
-        for (int i = tid; i <= a.B; i += kThreads)
+        for (int i = tid; i <= a.B; i += NT)
             a.hdr[2 + i] = P[i];
         if (tid == 0) {
             a.hdr[0] = T;
@@ -377,8 +380,10 @@ __global__ void __launch_bounds__(kMergeThreads * kMergeGroups) decode_merge_ker
 
 size_t decode_split_smem(bool e4m3, int B)
 {
-    const size_t tail = (size_t)(B + 1) * sizeof(int64_t) + kWarps * sizeof(int64_t);
-    return (e4m3 ? SmemPlan<true>::kTailOff : SmemPlan<false>::kTailOff) + tail;
+    const size_t tail = (size_t)(B + 1) * sizeof(int64_t) +
+                        (size_t)(e4m3 ? kDecodeWarps<true>() : kDecodeWarps<false>()) * sizeof(int64_t);
+    return (e4m3 ? SmemPlan<true, kDecodeWarps<true>()>::kTailOff
+                 : SmemPlan<false, kDecodeWarps<false>()>::kTailOff) + tail;
 }
 
 size_t workspace_bytes(int B, int Hkv, int C)
@@ -415,9 +420,11 @@ int split_ctas_per_sm(bool e4m3)
     if (e != cudaSuccess)
         return 1;
     if (e4m3)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_split_kernel<true>, kThreads, smem);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_split_kernel<true>,
+                                                          32 * kDecodeWarps<true>(), smem);
     else
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_split_kernel<false>, kThreads, smem);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_split_kernel<false>,
+                                                          32 * kDecodeWarps<false>(), smem);
     return (e == cudaSuccess && n > 0) ? n : 1;
 }
 
@@ -428,13 +435,14 @@ cudaError_t launch_decode(const DecodeArgs& a, bool e4m3, cudaStream_t s, void* 
         return e;
     const int grid = a.C > 0 ? a.C : a.B * a.Hkv;
     const size_t smem = a.C > 0 ? decode_split_smem(e4m3, a.B)
-                                : (e4m3 ? SmemPlan<true>::kTailOff : SmemPlan<false>::kTailOff);
+                                : (e4m3 ? SmemPlan<true, kDecodeWarps<true>()>::kTailOff
+                                        : SmemPlan<false, kDecodeWarps<false>()>::kTailOff);
     if (ev0 && ev1 && (e = cudaEventRecord((cudaEvent_t)ev0, s)) != cudaSuccess)
         return e;
     if (e4m3)
-        decode_split_kernel<true><<<grid, kThreads, smem, s>>>(a);
+        decode_split_kernel<true><<<grid, 32 * kDecodeWarps<true>(), smem, s>>>(a);
     else
-        decode_split_kernel<false><<<grid, kThreads, smem, s>>>(a);
+        decode_split_kernel<false><<<grid, 32 * kDecodeWarps<false>(), smem, s>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess)
         return e;
     if (ev0 && ev1 && (e = cudaEventRecord((cudaEvent_t)ev1, s)) != cudaSuccess)

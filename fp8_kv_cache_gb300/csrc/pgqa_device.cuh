@@ -40,7 +40,7 @@ constexpr int kD = 256;        // head dim (the only one built)
 constexpr int kGMax = 8;       // query heads per KV head, padded
 constexpr int kTile = 16;      // tokens per tile (unit of the split partition)
 constexpr int kHalf = 8;       // tokens per half-tile (unit of the warp pipeline)
-constexpr int kWarps = 4;      // warps per CTA
+constexpr int kWarps = 4;      // warps per CTA of the prefill kernels
 constexpr int kThreads = kWarps * 32;
 
 // One partial result of a split: m[8], l[8], O[8][256] (unnormalised), f32.
@@ -393,16 +393,14 @@ struct WarpCore {
         return kE4M3 ? 16 * g + 128 * (n >> 4) + (n & 15) : 8 * g + 64 * (n >> 3) + (n & 7);
     }
 
-    // The CTA's warps write the Q fragments of heads g < G (binary16 [G][256]
-    // rows at qg) into qs[16][32] (uint2), four k-steps each; the caller
-    // synchronises the CTA before use.
-    __device__ static void stage_q(uint2* qs, const __half* qg, int G, int lane, int w)
+    // The CTA's nw warps write the Q fragments of heads g < G (binary16
+    // [G][256] rows at qg) into qs[16][32] (uint2), the k-steps dealt to the
+    // warps in turn; the caller synchronises the CTA before use.
+    __device__ static void stage_q(uint2* qs, const __half* qg, int G, int lane, int w, int nw)
     {
         const int g = lane >> 2, q = lane & 3;
         const uint32_t* row = reinterpret_cast<const uint32_t*>(qg + (size_t)g * kD);
-#pragma unroll
-        for (int k = 0; k < 16 / kWarps; ++k) {
-            const int s = w * (16 / kWarps) + k;
+        for (int s = w; s < 16; s += nw) {
             uint2 f = make_uint2(0u, 0u);
             if (g < G) {
                 f.x = __ldg(row + (k_dim(q, 4 * s) >> 1));
@@ -582,44 +580,45 @@ __device__ __forceinline__ void run_tiles(WarpCore<kE4M3, kQRegs>& wc, WarpRing<
 // resolved block entries (int2 {first token, page} each), so that its ring
 // fills issue their copies without the two dependent global loads
 // (selection index, then block-table entry) in front of them.
-template <bool kE4M3>
+template <bool kE4M3, int NW = kWarps>
 struct SmemPlan {
     static constexpr int kNS = kStages<kE4M3>();
     static constexpr size_t kQBytes = (size_t)16 * 32 * sizeof(uint2);
-    static constexpr size_t kRingBytes = (size_t)kWarps * kNS * Stage<kE4M3>::kBytes;
+    static constexpr size_t kRingBytes = (size_t)NW * kNS * Stage<kE4M3>::kBytes;
     static constexpr size_t kMaskOff = kQBytes + kRingBytes;
-    static constexpr size_t kTailOff = (kMaskOff + (size_t)kWarps * kNS * 4 + 15) & ~(size_t)15;
+    static constexpr size_t kTailOff = (kMaskOff + (size_t)NW * kNS * 4 + 15) & ~(size_t)15;
     static constexpr int kPrefillEntries = kE4M3 ? 520 : 1024; // block entries per prefill chunk
     static constexpr size_t kPrefillSmem = kTailOff + (size_t)kPrefillEntries * sizeof(int2);
 };
 
 // ------------------------------------------------------------------ CTA merge
 
-// Combines the kWarps warps' states of one (row, KV head) through shared
-// memory.  Writes either the final binary16 output rows (out_rows != nullptr,
-// rows of the G heads at stride kD) or a partial slot (m, l, O).
+// Combines the NW warps' states of one (row, KV head) through shared memory.
+// Writes either the final binary16 output rows (out_rows != nullptr, rows of
+// the G heads at stride kD) or a partial slot (m, l, O).
+template <int NW = kWarps>
 struct MergeSmem {
-    float m[kWarps][kGMax];
-    float l[kWarps][kGMax];
-    float o[kWarps][kGMax][kD];
+    float m[NW][kGMax];
+    float l[NW][kGMax];
+    float o[NW][kGMax][kD];
 };
 
 // The pieces of a CTA's shared memory for one attention kernel instance.
-template <bool kE4M3>
+template <bool kE4M3, int NW = kWarps>
 struct CtaSmem {
-    uint2* qs;            // the CTA's Q fragments
-    MergeSmem* merge;     // aliases the rings; used only after every ring is drained
-    unsigned char* ring;  // this warp's ring
-    uint32_t* masks;      // this warp's stage masks
-    unsigned char* tail;  // kernel-specific tail
+    uint2* qs;              // the CTA's Q fragments
+    MergeSmem<NW>* merge;   // aliases the rings; used only after every ring is drained
+    unsigned char* ring;    // this warp's ring
+    uint32_t* masks;        // this warp's stage masks
+    unsigned char* tail;    // kernel-specific tail
 
     __device__ static CtaSmem carve(unsigned char* base, int w)
     {
-        using Pl = SmemPlan<kE4M3>;
-        static_assert(Pl::kRingBytes >= sizeof(MergeSmem), "merge buffer must fit in the rings");
+        using Pl = SmemPlan<kE4M3, NW>;
+        static_assert(Pl::kRingBytes >= sizeof(MergeSmem<NW>), "merge buffer must fit in the rings");
         CtaSmem c;
         c.qs = reinterpret_cast<uint2*>(base);
-        c.merge = reinterpret_cast<MergeSmem*>(base + Pl::kQBytes);
+        c.merge = reinterpret_cast<MergeSmem<NW>*>(base + Pl::kQBytes);
         c.ring = base + Pl::kQBytes + (size_t)w * Pl::kNS * Stage<kE4M3>::kBytes;
         c.masks = reinterpret_cast<uint32_t*>(base + Pl::kMaskOff) + w * Pl::kNS;
         c.tail = base + Pl::kTailOff;
@@ -627,9 +626,9 @@ struct CtaSmem {
     }
 };
 
-template <bool kE4M3, bool kQRegs = false>
-__device__ void cta_merge(MergeSmem& sm, const WarpCore<kE4M3, kQRegs>& wc, int G, float v_scale,
-                          __half* out_rows, float* slot)
+template <bool kE4M3, bool kQRegs = false, int NW = kWarps>
+__device__ void cta_merge(MergeSmem<NW>& sm, const WarpCore<kE4M3, kQRegs>& wc, int G,
+                          float v_scale, __half* out_rows, float* slot)
 {
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const int g = lane >> 2, q = lane & 3;
@@ -653,19 +652,19 @@ __device__ void cta_merge(MergeSmem& sm, const WarpCore<kE4M3, kQRegs>& wc, int 
     for (int h = 0; h < G; ++h) {
         float M = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < kWarps; ++i)
+        for (int i = 0; i < NW; ++i)
             M = fmaxf(M, sm.m[i][h]);
-        float sc[kWarps];
+        float sc[NW];
         float den = 0.f;
 #pragma unroll
-        for (int i = 0; i < kWarps; ++i) {
+        for (int i = 0; i < NW; ++i) {
             sc[i] = (M == -INFINITY) ? 0.f : ex2(sm.m[i][h] - M);
             den += sc[i] * sm.l[i][h];
         }
-        for (int d = tid; d < kD; d += kThreads) {
+        for (int d = tid; d < kD; d += NW * 32) {
             float num = 0.f;
 #pragma unroll
-            for (int i = 0; i < kWarps; ++i)
+            for (int i = 0; i < NW; ++i)
                 num += sc[i] * sm.o[i][h][d];
             if (out_rows != nullptr) {
                 const float v = den > 0.f ? num / den * v_scale : 0.f;

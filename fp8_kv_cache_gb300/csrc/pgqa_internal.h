@@ -15,6 +15,16 @@ constexpr int kMergeGroups = 4;       // groups of a merge CTA, taking chunks of
 constexpr int kMergeScanMax = 512;    // merge recomputes the cut from seq_lens up to this batch
 constexpr int kHeaderBytes = 64;       // workspace header: T, C_eff
 constexpr int kMaxDevices = 64;        // per-device caches
+// Warps of a decode CTA.  Four warps, with kMinCtas CTAs resident per SM
+// (3 for E4M3, 2 for FP16): one CTA per SM with all 12 (E4M3) or 8 (FP16)
+// warps measured within 2 % on the long decode and 3 to 6 % slower on short
+// ones, where more independent CTAs start more loads at once.
+template <bool kE4M3>
+__host__ __device__ constexpr int kDecodeWarps()
+{
+    return kWarps;
+}
+
 // Virtual tiles charged at the start of every non-empty segment when the tile
 // line is cut among the split CTAs: a CTA whose range takes in a segment start
 // runs one more piece (Q staging, pipeline start, CTA merge, about 5 us at

@@ -53,7 +53,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas<kE4M3>()) sparse_prefill_ke
     const CtaSmem<kE4M3> cs = CtaSmem<kE4M3>::carve(smem_raw, w);
     WarpRing<kE4M3, kStages<kE4M3>()> rg;
     rg.init(cs.ring, cs.masks);
-    Core::stage_q(cs.qs, a.q + ((size_t)r * a.Hq + (size_t)j * a.G) * kD, a.G, lane, w);
+    Core::stage_q(cs.qs, a.q + ((size_t)r * a.Hq + (size_t)j * a.G) * kD, a.G, lane, w, kWarps);
     Core wc;
     wc.reset();
     bool q_loaded = false;
