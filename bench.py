@@ -230,7 +230,7 @@ def run_ours(args, rank, world):
     stream = torch.cuda.current_stream()
 
     if args.phase == "prefill":
-        return run_prefill_only(args, dev)
+        return run_prefill_only(args, dev, route=1)
     if args.phase == "prefill-grouped":
         return run_prefill_only(args, dev, route=2)
     if args.phase == "select":
@@ -706,7 +706,7 @@ def prefill_roofline(pc, p_ms, g_ms, toks, gathered, flops, probe_ms, g_bytes, g
 
 def run_prefill_only(args, dev, route=0):
     """The sparse-prefill phase alone (for profiling); route as for
-    paged_gqa_sparse_prefill_route (0 = automatic, 2 = grouped)."""
+    paged_gqa_sparse_prefill_route (1 = per row, 2 = grouped)."""
     import torch
     import fp8_kv_cache_gb300 as P
     from fp8_kv_cache_gb300 import workloads as W
@@ -728,7 +728,7 @@ def run_prefill_only(args, dev, route=0):
         torch.cuda.synchronize()
         if i >= args.warmup:
             ms.append(a.elapsed_time(b))
-    return {"phase": "prefill" if route == 0 else "prefill-grouped", "ms": float(np.mean(ms))}
+    return {"phase": "prefill" if route == 1 else "prefill-grouped", "ms": float(np.mean(ms))}
 
 
 def run_select_only(args, dev):

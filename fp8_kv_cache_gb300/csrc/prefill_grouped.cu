@@ -22,13 +22,16 @@
 //     (K and V of 64 tokens, in the order K0 K1 K2 V0 K3 V1 ...) into the
 //     128-byte-swizzled K-major tile (see tc_device.cuh): FP16 rows by 16-byte
 //     cp.async, E4M3 rows through registers and the hardware converter.
-//   * one thread issues S = Q K^T (M = 128 slots, N = 64 tokens, K = 256; Q
-//     from TMEM, K from the stage) into one of two TMEM score buffers as soon
-//     as a buffer is free, and a thread of another warp issues O += P V
+//   * two threads in two warps issue S = Q K^T (M = 128 slots, N = 64
+//     tokens, K = 256; Q from TMEM, K from the stage), one for the even and
+//     one for the odd stages, each into its own TMEM score buffer as soon as
+//     that buffer is free, and a thread of a third warp issues O += P V
 //     (M = 128, N = 256, K = 64; P from shared memory, V from the stage bytes
 //     read as an MN-major operand) into a 256-column TMEM accumulator once a
 //     stage's probabilities are written, so Q K^T runs ahead of the softmax
-//     without waiting behind P V.
+//     without waiting behind P V.  Each issuer counts its own phases of every
+//     ring slot (K barriers per parity, a V barrier per slot), so no waiter
+//     ever runs two phases ahead of a barrier.
 //   * 8 softmax warps in two warpgroups that take alternate stages (A the
 //     even ones, B the odd ones), so one group's exponentials and stores
 //     overlap the other's score reads.  A thread owns one slot (its TMEM
