@@ -60,6 +60,7 @@ struct SelectShared {
     int32_t warp_gt[kWarps];
     int32_t warp_eq[kWarps];
     int32_t pick_digit, pick_above, pick_count;
+    uint32_t low_and, low_or;        // AND / OR of bits 9..0 over the first digit's bucket
 };
 
 // Keys of a row: staged in shared memory or read from global memory.
@@ -141,6 +142,63 @@ __device__ __forceinline__ int block_exclusive_scan(Sh& sh, int v, int& total)
     return base + incl - v;
 }
 
+// Digits 2 (bits 20..10) and 3 (bits 9..0) of the pivot, from the keys
+// key_at(0 .. m) that match prefix/mask (the first digit): need is the rank
+// of the pivot among them on entry and among its equals on return; prefix and
+// mask then cover every fixed bit.  When the keys matching the first digit
+// all share bits 9..0 (known from an AND and an OR taken in the second pass),
+// so do those matching the first two, and the third pass is skipped: those
+// bits are the pivot's.  Starts with a CTA barrier; every thread leaves after
+// the same last one.
+template <class Sh, class KeyAt>
+__device__ __forceinline__ void later_digits(Sh& sh, const KeyAt& key_at, int m, int& need,
+                                             uint32_t& prefix, uint32_t& mask)
+{
+    const int tid = threadIdx.x, lane = tid & 31;
+#pragma unroll 1
+    for (int pass = 0; pass < 2; ++pass) {
+        const int shift = pass == 0 ? 10 : 0;
+        const uint32_t dmask = pass == 0 ? 2047u : 1023u;
+        __syncthreads();                              // list and previous picks complete
+        for (int i = tid; i < kBins; i += Sh::kThreads)
+            sh.hist[i] = 0;
+        if (tid == 0) {
+            sh.low_and = 0xFFFFFFFFu;
+            sh.low_or = 0u;
+        }
+        __syncthreads();
+        uint32_t land = 0xFFFFFFFFu, lor = 0u;
+        for (int j = tid; j < m; j += Sh::kThreads) {
+            const uint32_t kv = key_at(j);
+            if ((kv & mask) == prefix) {
+                atomicAdd(&sh.hist[(kv >> shift) & dmask], 1u);
+                land &= kv;
+                lor |= kv;
+            }
+        }
+        if (pass == 0) {
+            land = __reduce_and_sync(0xffffffffu, land & 1023u);
+            lor = __reduce_or_sync(0xffffffffu, lor & 1023u);
+            if (lane == 0) {
+                atomicAnd(&sh.low_and, land);
+                atomicOr(&sh.low_or, lor);
+            }
+        }
+        __syncthreads();
+        pick_digit(sh, pass == 0 ? kBins : 1024, need);
+        need -= sh.pick_above;
+        prefix |= (uint32_t)sh.pick_digit << shift;
+        mask |= dmask << shift;
+        if (sh.pick_count == need)
+            break;                                    // CTA-uniform
+        if (pass == 0 && sh.low_and == sh.low_or) {   // CTA-uniform: bits 9..0 are shared
+            prefix |= sh.low_and;
+            mask |= 1023u;
+            break;
+        }
+    }
+}
+
 // Fast path of radix_select for rows of n <= 32 kMapWords keys whose
 // first-digit bucket fits the list: bitmaps instead of ordered sweeps.
 //   above_map  keys whose first digit is above the pivot's (all taken);
@@ -156,6 +214,7 @@ __device__ void select_by_bitmaps(const Keys& key, int n, int32_t* out, Sh& sh,
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const int nw = (n + 31) >> 5;
     // ---- one sweep: ballots of 32 consecutive keys are the bitmap words
+#pragma unroll 4
     for (int wd = w; wd < nw; wd += Sh::kWarps) {
         const int i = 32 * wd + lane;
         const uint32_t b = i < n ? key(i) >> 21 : 0u;
@@ -189,27 +248,7 @@ __device__ void select_by_bitmaps(const Keys& key, int n, int32_t* out, Sh& sh,
         }
         // ---- later digits over the bucket
         uint32_t prefix = d1 << 21, mask = 0xFFE00000u;
-#pragma unroll 1
-        for (int pass = 0; pass < 2; ++pass) {
-            const int shift = pass == 0 ? 10 : 0;
-            const uint32_t dmask = pass == 0 ? 2047u : 1023u;
-            __syncthreads();                              // list complete / picks read
-            for (int i = tid; i < kBins; i += Sh::kThreads)
-                sh.hist[i] = 0;
-            __syncthreads();
-            for (int j = tid; j < count1; j += Sh::kThreads) {
-                const uint32_t kv = key(sh.list[j]);
-                if ((kv & mask) == prefix)
-                    atomicAdd(&sh.hist[(kv >> shift) & dmask], 1u);
-            }
-            __syncthreads();
-            pick_digit(sh, pass == 0 ? kBins : 1024, need);
-            need -= sh.pick_above;
-            prefix |= (uint32_t)sh.pick_digit << shift;
-            mask |= dmask << shift;
-            if (sh.pick_count == need)
-                break;                                    // CTA-uniform
-        }
+        later_digits(sh, [&](int j) { return key(sh.list[j]); }, count1, need, prefix, mask);
         // ---- taken bucket keys: contiguous list ranges per thread, ties by index
         const int lper = (count1 + Sh::kThreads - 1) / Sh::kThreads;
         const int j0 = min(count1, tid * lper), j1 = min(count1, j0 + lper);
@@ -349,35 +388,10 @@ __device__ void radix_select(const uint32_t* row, uint32_t* stage, const Keys& k
 
     if (!done1) {
         // ---- digits 2 (bits 20..10) and 3 (bits 9..0) over the bucket
-#pragma unroll 1
-        for (int pass = 0; pass < 2; ++pass) {
-            const int shift = pass == 0 ? 10 : 0;
-            const uint32_t dmask = pass == 0 ? 2047u : 1023u;
-            __syncthreads();                              // list and previous picks complete
-            for (int i = tid; i < kBins; i += Sh::kThreads)
-                sh.hist[i] = 0;
-            __syncthreads();
-            if (use_list) {
-                for (int j = tid; j < count1; j += Sh::kThreads) {
-                    const uint32_t kv = key(sh.list[j]);
-                    if ((kv & mask) == prefix)
-                        atomicAdd(&sh.hist[(kv >> shift) & dmask], 1u);
-                }
-            } else {
-                for (int i = tid; i < n; i += Sh::kThreads) {
-                    const uint32_t kv = key(i);
-                    if ((kv & mask) == prefix)
-                        atomicAdd(&sh.hist[(kv >> shift) & dmask], 1u);
-                }
-            }
-            __syncthreads();
-            pick_digit(sh, pass == 0 ? kBins : 1024, need);
-            need -= sh.pick_above;
-            prefix |= (uint32_t)sh.pick_digit << shift;
-            mask |= dmask << shift;
-            if (sh.pick_count == need)
-                break;                                    // CTA-uniform
-        }
+        if (use_list)
+            later_digits(sh, [&](int j) { return key(sh.list[j]); }, count1, need, prefix, mask);
+        else
+            later_digits(sh, key, n, need, prefix, mask);
         // ---- per-warp counts of the bucket's keys above / at the pivot
         if (use_list) {
             for (int j = tid; j < count1; j += Sh::kThreads) {
