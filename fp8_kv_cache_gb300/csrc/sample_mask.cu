@@ -7,8 +7,8 @@
 // logits (equal logits: the lower index first); top-p keeps, of those in that
 // order, the shortest leading run whose softmax mass (over the top-k logits)
 // reaches p; every other logit becomes -infinity.  The top-p mass is computed
-// in FP64: e_j = exp(x_j - x_0), suffix sums S_j = e_j + S_{j+1} from the end
-// of the list, logit j kept iff S_j > (1 - p) S_0.
+// in FP64: e_j = exp(x_j - x_0), suffix sums S_j = e_j + S_{j+1} of the list
+// (formed by a shuffle scan here), logit j kept iff S_j > (1 - p) S_0.
 //
 // Design (ours): one thread-block cluster of kMaskCtas CTAs per row, so a
 // handful of rows still spreads over the GPU.  Each CTA sweeps its slice of

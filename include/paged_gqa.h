@@ -342,9 +342,11 @@ int paged_gqa_select_blocks(const float* scores, int64_t score_stride, int n_blo
  * largest (equal logits: the lower index first); top-p keeps, of those in
  * that order, the shortest leading run whose probability mass reaches p, the
  * probabilities being the softmax over the top-k logits, computed in FP64:
- * e_j = exp(x_j - x_0), S_j = e_j + S_{j+1} summed from the end of the list,
- * logit j kept iff S_j > (1 - p) S_0.  out = the kept logits, bit for bit,
- * and -infinity everywhere else.
+ * e_j = exp(x_j - x_0), S_j = e_j + e_{j+1} + ... (the suffix sums of the
+ * list, added in FP64 by a parallel scan: they may differ from a serial sum
+ * from the end by a few units in the last place), logit j kept iff
+ * S_j > (1 - p) S_0.  out = the kept logits, bit for bit, and -infinity
+ * everywhere else.
  *
  *  logits        device float32; row b starts at logits + b * logits_stride
  *                (>= V, in elements).  Finite or -inf values; a row whose
