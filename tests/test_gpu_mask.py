@@ -102,6 +102,32 @@ def test_strided_and_in_place():
     assert np.array_equal(b.view(np.uint32), want.view(np.uint32))
 
 
+def test_unaligned_output_rows_and_in_place_unaligned_rows():
+    """An output whose rows start off a 16-byte boundary (the -inf fill is
+    then written by the threads during the sweep, not by bulk copies), and
+    masking in place rows that start off a 16-byte boundary."""
+    import torch
+    import fp8_kv_cache_gb300 as P
+    c = W.logits_case("unaligned_out", B=5, V=30001, seed=507)
+    want, margin = oracle.topk_topp_mask(c.logits, 20, 0.95)
+    x = torch.from_numpy(c.logits).cuda()
+    big = torch.full((5, 30001 + 3), 5.0, dtype=torch.float32, device="cuda")
+    out = big[:, 1:30002]                                  # rows at 4 bytes past an aligned start
+    assert out.data_ptr() % 16 != 0
+    P.paged_gqa_topk_topp_mask(x, 20, 0.95, out=out)
+    buf = torch.full((5, 30007), 7.0, dtype=torch.float32, device="cuda")
+    xs = buf[:, 1:30002]
+    xs.copy_(x)
+    P.paged_gqa_topk_topp_mask(xs, 20, 0.95, out=xs)      # in place, odd row stride
+    torch.cuda.synchronize()
+    for got in (out.cpu().numpy(), xs.cpu().numpy()):
+        for r in range(5):
+            if not np.array_equal(got[r].view(np.uint32), want[r].view(np.uint32)):
+                assert margin[r] < MARGIN, f"row {r}"
+    assert bool((big[:, 0] == 5.0).all()) and bool((big[:, 30002:] == 5.0).all())
+    assert bool((buf[:, 0] == 7.0).all()) and bool((buf[:, 30002:] == 7.0).all())
+
+
 def test_nan_or_inf_top_is_flagged():
     rng = np.random.default_rng(504)
     x = rng.standard_normal((3, 1000)).astype(np.float32)
