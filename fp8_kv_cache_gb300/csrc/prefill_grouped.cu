@@ -368,9 +368,11 @@ __device__ __forceinline__ int64_t stage_block_offset(const GroupArgs& ga, const
 // stage's 16 blocks (rank -> block -> page) in parallel, for the warp's next
 // stage while the current one's copies are in flight.  FP16 rows: each lane
 // copies its 16-byte chunk of all 64 rows with cp.async and waits for its
-// own copies.  E4M3 rows (256 codes): each lane loads 16-code chunks into
-// registers, converts them exactly to binary16 with the hardware converter
-// and stores the two 16-byte halves into the same tile layout.  The warp then
+// own copies.  E4M3 rows (256 codes, half the bytes): the codes go by
+// cp.async into the upper half of the slot, all in flight at once; the warp
+// then holds codes 128..255 in registers, converts codes 0..127 exactly to
+// binary16 (hardware converter) into the lower half of the tile layout, and
+// after a warp barrier writes the held half over the raw codes.  The warp then
 // fences its writes for the tensor cores and publishes the stage on the
 // barrier of its kind; stages of different warps are in flight together.
 template <bool kE4M3>
@@ -402,36 +404,69 @@ __device__ void produce(const GroupArgs& ga, Smem& sm, Cursor& cur, int j, int n
             stage_of(qn, nt, nv, nh);
         int64_t off_next = -1;
         if (kE4M3) {
-            // chunk idx = lane + 32 i: row idx / 16, codes 16 (idx % 16) .. + 15
+            // The stage's raw codes (64 rows x 256 bytes) go by cp.async into
+            // the upper half of the slot, linearly (row t at 16 KB + 256 t), all
+            // in flight at once.  Chunk idx = lane + 32 i: row idx / 16, codes
+            // 16 (idx % 16) .. + 15.
             const uint32_t st = tc::smem_addr(sm.ring[s]);
-#pragma unroll 1
-            for (int part = 0; part < 4; ++part) {
-                uint4 raw[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int idx = lane + 32 * (8 * part + i), row = idx >> 4;
-                    const int64_t o = __shfl_sync(0xffffffffu, off, row >> 2);
-                    raw[i] = o < 0 ? make_uint4(0u, 0u, 0u, 0u)
-                                   : ldg_stream(base + o + (row & 3) * a.kv.token_b + 16 * (idx & 15));
-                }
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int idx = lane + 32 * (8 * part + i), row = idx >> 4, c16 = idx & 15;
-                    uint32_t h[8];
-                    e4m3x4_to_f16x2x2(raw[i].x, h[0], h[1]);
-                    e4m3x4_to_f16x2x2(raw[i].y, h[2], h[3]);
-                    e4m3x4_to_f16x2x2(raw[i].z, h[4], h[5]);
-                    e4m3x4_to_f16x2x2(raw[i].w, h[6], h[7]);
-                    const uint32_t rb = st + (c16 >> 2) * kRegionBytes + row * 128;
-                    const uint32_t x0 = 2 * (c16 & 3);
-                    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(rb + ((x0 ^ (row & 7)) << 4)),
-                                 "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3]) : "memory");
-                    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(rb + (((x0 + 1) ^ (row & 7)) << 4)),
-                                 "r"(h[4]), "r"(h[5]), "r"(h[6]), "r"(h[7]) : "memory");
-                }
+            const uint32_t raw = st + kStageBytes / 2;
+#pragma unroll 8
+            for (int i = 0; i < 32; ++i) {
+                const int idx = lane + 32 * i, row = idx >> 4;
+                const int64_t o = __shfl_sync(0xffffffffu, off, row >> 2);
+                const unsigned char* src =
+                    base + (o < 0 ? 0 : o + (row & 3) * a.kv.token_b + 16 * (idx & 15));
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(raw + 16 * idx),
+                             "l"(src), "r"(o < 0 ? 0 : 16)
+                             : "memory");
             }
-            if (qn < n)
+            cp_async_commit();
+            if (qn < n)                          // the next stage's rows, while these copies fly
                 off_next = stage_block_offset(ga, sm, j, nbw, n_union, nh, lane);
+            cp_async_wait<0>();
+            __syncwarp();
+            // codes 128..255 of every row into registers (chunk idx = lane +
+            // 32 i: row idx / 8, codes 128 + 16 (idx % 8) .. + 15), so the
+            // f16 tiles of dimensions 128..255 may overwrite the raw half
+            uint4 hi[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int idx = lane + 32 * i;
+                asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                             : "=r"(hi[i].x), "=r"(hi[i].y), "=r"(hi[i].z), "=r"(hi[i].w)
+                             : "r"(raw + 256 * (idx >> 3) + 128 + 16 * (idx & 7)));
+            }
+            // 16 codes (chunk c16 of row `row`) -> two 16-byte f16 chunks of the
+            // 128-byte-swizzled K-major tile
+            auto put = [&](const uint4& r4, int row, int c16) {
+                uint32_t h[8];
+                e4m3x4_to_f16x2x2(r4.x, h[0], h[1]);
+                e4m3x4_to_f16x2x2(r4.y, h[2], h[3]);
+                e4m3x4_to_f16x2x2(r4.z, h[4], h[5]);
+                e4m3x4_to_f16x2x2(r4.w, h[6], h[7]);
+                const uint32_t rb = st + (c16 >> 2) * kRegionBytes + row * 128;
+                const uint32_t x0 = 2 * (c16 & 3);
+                asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(rb + ((x0 ^ (row & 7)) << 4)),
+                             "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3]) : "memory");
+                asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(rb + (((x0 + 1) ^ (row & 7)) << 4)),
+                             "r"(h[4]), "r"(h[5]), "r"(h[6]), "r"(h[7]) : "memory");
+            };
+            // dimensions 0..127 into the lower half, read from the raw half
+#pragma unroll 4
+            for (int i = 0; i < 16; ++i) {
+                const int idx = lane + 32 * i, row = idx >> 3, c16 = idx & 7;
+                uint4 r4;
+                asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                             : "=r"(r4.x), "=r"(r4.y), "=r"(r4.z), "=r"(r4.w)
+                             : "r"(raw + 256 * row + 16 * c16));
+                put(r4, row, c16);
+            }
+            __syncwarp();                        // every lane is done with the raw half
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int idx = lane + 32 * i;
+                put(hi[i], idx >> 3, 8 + (idx & 7));
+            }
         } else {
             const uint32_t st = tc::smem_addr(sm.ring[s]) + (lane >> 3) * kRegionBytes;
             const uint32_t x = lane & 7;
