@@ -233,6 +233,8 @@ def run_ours(args, rank, world):
         return run_prefill_only(args, dev, route=1)
     if args.phase == "prefill-grouped":
         return run_prefill_only(args, dev, route=2)
+    if args.phase == "prefill-grouped-e4m3":
+        return run_prefill_only(args, dev, route=2, kv_dtype="e4m3")
     if args.phase == "select":
         return run_select_only(args, dev)
     if args.phase == "mask":
@@ -704,13 +706,14 @@ def prefill_roofline(pc, p_ms, g_ms, toks, gathered, flops, probe_ms, g_bytes, g
             "bound": "L2 -> shared-memory gather (the 32 MiB cache stays in L2)"}
 
 
-def run_prefill_only(args, dev, route=0):
+def run_prefill_only(args, dev, route=0, kv_dtype="fp16"):
     """The sparse-prefill phase alone (for profiling); route as for
-    paged_gqa_sparse_prefill_route (1 = per row, 2 = grouped)."""
+    paged_gqa_sparse_prefill_route (1 = per row, 2 = grouped), over the FP16
+    cache or its E4M3 copy."""
     import torch
     import fp8_kv_cache_gb300 as P
     from fp8_kv_cache_gb300 import workloads as W
-    pc = W.sparse_prefill_4096()
+    pc = W.sparse_prefill_4096(kv_dtype=kv_dtype)
     pkv = torch.from_numpy(pc.kv).to(dev)
     pk, pv = pkv[:, :, :, 0, :], pkv[:, :, :, 1, :]
     pq = torch.from_numpy(pc.q).to(dev)
@@ -728,7 +731,8 @@ def run_prefill_only(args, dev, route=0):
         torch.cuda.synchronize()
         if i >= args.warmup:
             ms.append(a.elapsed_time(b))
-    return {"phase": "prefill" if route == 1 else "prefill-grouped", "ms": float(np.mean(ms))}
+    return {"phase": ("prefill" if route == 1 else "prefill-grouped")
+                      + ("" if kv_dtype == "fp16" else "-" + kv_dtype), "ms": float(np.mean(ms))}
 
 
 def run_select_only(args, dev):
@@ -851,7 +855,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--phase", choices=["all", "decode", "prefill", "prefill-grouped", "select",
+    ap.add_argument("--phase", choices=["all", "decode", "prefill", "prefill-grouped",
+                                        "prefill-grouped-e4m3", "select",
                                         "mask"],
                     default="all",
                     help="run only one phase (for profiling); the JSON line needs 'all'")
