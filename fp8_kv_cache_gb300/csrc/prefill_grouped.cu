@@ -18,18 +18,18 @@
 //     sequence's blocks; a prefix popcount ranks the union; each row gets a
 //     16-bit mask per 64-token stage saying which of the stage's 16 blocks it
 //     attends (its own block limited to positions <= p); Q goes to TMEM.
-//   * 5 producer warps, one per slot of a 5-stage ring, gather whole stages
-//     (K and V of 64 tokens, in the order K0 K1 K2 V0 K3 V1 ...) into the
+//   * 5 producer warps take turns over a 6-stage ring, gathering whole
+//     stages (K and V of 64 tokens, in the order K0 K1 V0 K2 V1 ...) into the
 //     128-byte-swizzled K-major tile (see tc_device.cuh): FP16 rows by 16-byte
-//     cp.async, E4M3 rows through registers and the hardware converter.
+//     cp.async, E4M3 codes by cp.async into the slot and converted in place.
 //   * two threads in two warps issue S = Q K^T (M = 128 slots, N = 64
 //     tokens, K = 256; Q from TMEM, K from the stage), one for the even and
 //     one for the odd stages, each into its own TMEM score buffer as soon as
 //     that buffer is free, and a thread of a third warp issues O += P V
-//     (M = 128, N = 256, K = 64; P from shared memory, V from the stage bytes
-//     read as an MN-major operand) into a 256-column TMEM accumulator once a
-//     stage's probabilities are written, so Q K^T runs ahead of the softmax
-//     without waiting behind P V.  Each issuer counts its own phases of every
+//     (M = 128, N = 256, K = 64; P from TMEM, V from the stage bytes read as
+//     an MN-major operand) into a 256-column TMEM accumulator once a stage's
+//     probabilities are written, so Q K^T runs ahead of the softmax without
+//     waiting behind P V.  Each issuer counts its own phases of every
 //     ring slot (K barriers per parity, a V barrier per slot), so no waiter
 //     ever runs two phases ahead of a barrier.
 //   * 8 softmax warps in two warpgroups that take alternate stages (A the
@@ -42,7 +42,10 @@
 //     groups).  The reference grows only when a stage's maximum exceeds it
 //     by more than 2^8, and then O is rescaled in TMEM; each group keeps its
 //     own sum under the reference it last saw, so the result is exact up to
-//     rounding.  FP16 probabilities go to shared memory for P V.
+//     rounding.  The FP16 probabilities go back into TMEM over the first 32
+//     columns of the stage's score buffer (its scores are in registers by
+//     then), so no shared memory holds P and the ring has a sixth slot; a
+//     score buffer is reused by Q K^T once P V has read the P in it.
 // Masked-out (slot, token) pairs cost tensor-core work but no memory traffic;
 // on the 4096-row workload the union is 0.60 of the per-row gather.  Groups
 // are sized so the units fill whole waves of one CTA per SM and are dealt in
@@ -62,11 +65,11 @@ namespace grp {
 constexpr int kM = kGroupSlots;               // query-head slots of a group (MMA M)
 constexpr int kStageTokens = 64;             // tokens per stage: 16 four-token blocks
 constexpr int kStageBlocks = 16;
-constexpr int kNS = 5;                       // ring stages, one producer warp each
+constexpr int kNS = 6;                       // ring stages
 constexpr int kRegionBytes = kStageTokens * 128;      // 64 head-dim columns of a stage
 constexpr int kStageBytes = kStageTokens * kD * 2;    // 32 KB
 constexpr int kMaskWords = 4096;             // 16 KB of per-row stage masks
-constexpr int kSoftWarps = 8, kMmaWarp = 8, kProdWarps = kNS, kProdWarp0 = 9;
+constexpr int kSoftWarps = 8, kMmaWarp = 8, kProdWarps = 5, kProdWarp0 = 9;
 constexpr int kPvWarp = kProdWarp0 + kProdWarps;   // issues P V
 constexpr int kQkWarp1 = kPvWarp + 1;               // with kMmaWarp: Q K^T of odd / even stages
 constexpr int kThreads = 32 * (kSoftWarps + 1 + kProdWarps + 2);
@@ -74,13 +77,12 @@ constexpr int kGroupThreads = kSoftWarps / 2 * 32;   // one softmax warpgroup
 constexpr float kRescaleSlack = 8.f;         // log2-domain growth tolerated before rescaling O
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemQ = 0;               // Q: 128 columns of f16 pairs
-constexpr uint32_t kTmemS = 128;             // S buffers at 128 and 192 (64 columns each)
+constexpr uint32_t kTmemS = 128;             // S buffers at 128 and 192 (64 columns each);
+                                             // P of a stage overwrites its first 32 columns
 constexpr uint32_t kTmemO = 256;             // O: 256 f32 columns
-constexpr int kPBytes = kM * 128;            // one P buffer: 128 slots x 64 tokens, K-major
 
 struct Smem {
     unsigned char ring[kNS][kStageBytes];
-    unsigned char p[2][kPBytes];             // FP16 probabilities, the A operand of P V
     uint32_t bitmap[kGroupMaxWords];         // union of the group's blocks
     int rank[kGroupMaxWords];                // exclusive prefix popcount of bitmap
     uint32_t masks[kMaskWords];              // [row][stage / 2]: two 16-bit stage masks per word
@@ -96,13 +98,21 @@ struct Smem {
     // phase of its barriers in order: a parity wait is only unambiguous
     // while its barrier is at most one phase behind.
     uint32_t taken[3][kNS];
-    uint64_t s_full[2], s_free[2], p_full[2], p_free[2], done;
+    // Uses of each ring slot published so far.  Consecutive uses of a slot
+    // come from different producer warps (stage it: warp it % kProdWarps,
+    // slot it % kNS), so the producer of use u first waits until use u - 1
+    // is published: its producer had waited for use u - 2 to be consumed,
+    // which keeps the slot's empty barrier at most one phase behind the
+    // parity this producer waits for.
+    uint32_t slot_pub[kNS];
+    uint64_t s_full[2], p_full[2], p_free[2], done;
     uint32_t tmem_base;
     int flags, n_union, abort;
     long spin_limit;
 };
 
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;   // + alignment of the tiles
+static_assert(kSmemBytes <= 232448, "shared memory above the per-CTA opt-in limit");
 
 // Where a unit's loop stands; every role walks the same sequence, so the
 // global counters agree between roles without communication.
@@ -123,6 +133,22 @@ __device__ __forceinline__ void wait_or_abort(Smem& sm, uint64_t* bar, uint32_t 
         return;
     if (!tc::mbar_wait(bar, par, sm.spin_limit))
         *ab = 1;
+}
+
+// Bounded wait until `uses` uses of ring slot s are published (a counter
+// other producer warps of this CTA write); skipped, like the mbarrier waits,
+// once any wait of the CTA has timed out.
+__device__ __forceinline__ void wait_published(Smem& sm, int s, uint32_t uses)
+{
+    volatile int* ab = &sm.abort;
+    const volatile uint32_t* pub = &sm.slot_pub[s];
+    for (long n = 0; !*ab && *pub < uses; ++n) {
+        if (n >= sm.spin_limit) {
+            *ab = 1;
+            return;
+        }
+        __nanosleep(64);
+    }
 }
 
 __device__ __forceinline__ bool page_valid_block(const KVGeom& g, const int32_t* bt, int b,
@@ -363,8 +389,9 @@ __device__ __forceinline__ int64_t stage_block_offset(const GroupArgs& ga, const
     return off;
 }
 
-// Producer warps: warp pw owns ring slot pw and fills every stage that lands
-// there (positions q with (it0 + q) % kNS == pw): lanes 0..15 resolve the
+// Producer warps: warp pw fills the stages it = pw, pw + kProdWarps, ... of
+// the ring (slot it % kNS; the warp waits until the slot's previous use is
+// published, then consumed): lanes 0..15 resolve the
 // stage's 16 blocks (rank -> block -> page) in parallel, for the warp's next
 // stage while the current one's copies are in flight.  FP16 rows: each lane
 // copies its 16-byte chunk of all 64 rows with cp.async and waits for its
@@ -383,7 +410,7 @@ __device__ void produce(const GroupArgs& ga, Smem& sm, Cursor& cur, int j, int n
     const int lane = threadIdx.x & 31, pw = (threadIdx.x >> 5) - kProdWarp0;
     const uint32_t it0 = cur.it;
     const int n = 2 * nt;
-    int q = (pw - (int)(it0 % kNS) + kNS) % kNS;
+    int q = (pw - (int)(it0 % kProdWarps) + kProdWarps) % kProdWarps;
     bool is_v = false;
     int ht = 0;
     int64_t off = -1;
@@ -391,13 +418,16 @@ __device__ void produce(const GroupArgs& ga, Smem& sm, Cursor& cur, int j, int n
         stage_of(q, nt, is_v, ht);
         off = stage_block_offset(ga, sm, j, nbw, n_union, ht, lane);
     }
-    for (; q < n; q += kNS) {
+    for (; q < n; q += kProdWarps) {
         const uint32_t it = it0 + q;
-        const int s = pw;
-        if (it >= (uint32_t)kNS)
-            wait_or_abort(sm, &sm.empty[s], ((it / kNS) - 1) & 1);
+        const int s = (int)(it % kNS);
+        const uint32_t use = it / kNS;       // this stage is use `use` of slot s
+        if (use > 0) {
+            wait_published(sm, s, use);      // use - 1 is in the slot (or was)
+            wait_or_abort(sm, &sm.empty[s], (use - 1) & 1);
+        }
         const unsigned char* base = is_v ? a.kv.v : a.kv.k;
-        const int qn = q + kNS;
+        const int qn = q + kProdWarps;
         bool nv = false;
         int nh = 0;
         if (qn < n)
@@ -489,8 +519,12 @@ __device__ void produce(const GroupArgs& ga, Smem& sm, Cursor& cur, int j, int n
             cp_async_wait<0>();
         }
         tc::fence_async_shared();
-        if ((int)it != ga.stall_stage)       // test hook: a stage left unpublished
+        if ((int)it != ga.stall_stage) {     // test hook: a stage left unpublished
             tc::mbar_arrive(is_v ? &sm.full_v[s] : &sm.full_k[ht & 1][s]);
+            __syncwarp();
+            if (lane == 0)
+                *reinterpret_cast<volatile uint32_t*>(&sm.slot_pub[s]) = use + 1;
+        }
         off = off_next;
         is_v = nv;
         ht = nh;
@@ -518,8 +552,8 @@ __device__ void issue_qk(Smem& sm, Cursor& cur, int nt, int par)
         const uint32_t g = g0 + ht, buf = g & 1, s = cur.it % kNS;
         const uint32_t st = tc::smem_addr(sm.ring[s]);
         wait_or_abort(sm, &sm.full_k[par][s], sm.taken[par][s]++ & 1);
-        if (g >= 2)
-            wait_or_abort(sm, &sm.s_free[buf], ((g >> 1) - 1) & 1);
+        if (g >= 2)                          // P V of stage g - 2 has read P (and so S) there
+            wait_or_abort(sm, &sm.p_free[buf], ((g >> 1) - 1) & 1);
         tc::fence_after_sync();
         // descriptors advance by their 16-byte address field: K steps of
         // 16 elements are 32 bytes inside a row, every 4th a new region
@@ -552,13 +586,14 @@ __device__ void issue_pv(Smem& sm, Cursor& cur, int nt)
         wait_or_abort(sm, &sm.full_v[s], sm.taken[2][s]++ & 1);
         wait_or_abort(sm, &sm.p_full[buf], (g >> 1) & 1);
         tc::fence_after_sync();
-        const uint64_t da0 = tc::sw128_desc(tc::smem_addr(sm.p[buf]), 16, 1024);
         const uint64_t db0 = tc::sw128_desc(st, kRegionBytes, 1024);
         const uint32_t acc0 = ht > 0;
+        // P (128 slots x 64 tokens, f16 pairs) from the first 32 columns of
+        // the stage's score buffer; 16 tokens per K step = 8 columns
 #pragma unroll
         for (int kk = 0; kk < kStageTokens / 16; ++kk)
-            tc::mma_ss(tm + kTmemO, da0 + (uint64_t)(kk * 2), db0 + (uint64_t)(kk * 128), kIdPV,
-                       kk > 0 ? 1u : acc0);
+            tc::mma_ts(tm + kTmemO, tm + kTmemS + 64 * buf + 8 * kk,
+                       db0 + (uint64_t)(kk * 128), kIdPV, kk > 0 ? 1u : acc0);
         tc::mma_commit(&sm.empty[s]);
         tc::mma_commit(&sm.p_free[buf]);
     }
@@ -582,27 +617,35 @@ __device__ int listed_count(const PrefillArgs& a, int r, int b, int own)
 // attended block of the stage (first union rank k0) in the slot's P row are
 // multiplied by the number of times the row lists the block; returns the
 // probability mass this adds to the row's sum.
-__device__ __noinline__ float scale_listed(const PrefillArgs& a, const Smem& sm,
-                                           unsigned char* prow, int slot, int r, int own, int nbw,
-                                           int k0, uint32_t live16)
+// Duplicated selections (a caller error) keep their meaning -- a block
+// listed c times counts c times: the probabilities of this thread's slot in
+// the stage's P (32 TMEM columns of f16 pairs at taddr, just stored) are
+// multiplied by their blocks' listing counts; returns the mass added.
+// Warp-collective (TMEM loads and stores are): lanes without duplicates
+// write their row back unchanged.
+__device__ __noinline__ float scale_listed(const PrefillArgs& a, const Smem& sm, uint32_t taddr,
+                                           bool dup, int r, int own, int nbw, int k0,
+                                           uint32_t live16)
 {
+    uint32_t pk[32];
+    tc::tmem_wait_st();                        // the stores just issued, before reading them
+    tc::tmem_ld32(taddr, pk);
+    tc::tmem_wait_ld();
     float added = 0.f;
-    for (int kb = 0; kb < kStageBlocks; ++kb) {
+    for (int kb = 0; dup && kb < kStageBlocks; ++kb) {
         if (!((live16 >> kb) & 1u))
             continue;
         const int cnt = listed_count(a, r, block_of_rank(sm, nbw, k0 + kb), own);
         if (cnt == 1)
             continue;
-        __half2* h = reinterpret_cast<__half2*>(prow + (((kb >> 1) ^ (slot & 7)) << 4) +
-                                                8 * (kb & 1));
-#pragma unroll
         for (int e = 0; e < 2; ++e) {
-            const float2 f = __half22float2(h[e]);
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&pk[2 * kb + e]));
             const float p0 = f.x * (float)cnt, p1 = f.y * (float)cnt;
             added += (p0 + p1) - (f.x + f.y);
-            h[e] = __floats2half2_rn(p0, p1);
+            pk[2 * kb + e] = pack_half2(p0, p1);
         }
     }
+    tc::tmem_st32(taddr, pk);
     return added;
 }
 
@@ -674,8 +717,6 @@ __device__ void softmax_unit(const GroupArgs& ga, Smem& sm, Cursor& cur, int r0,
         tc::tmem_ld32(tl + kTmemS + 64 * buf, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
         tc::tmem_ld32(tl + kTmemS + 64 * buf + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
         tc::tmem_wait_ld();
-        tc::fence_before_sync();
-        tc::mbar_arrive(&sm.s_free[buf]);      // Q K^T of stage g + 2 may overwrite S
 
         float x[64];
 #pragma unroll
@@ -721,12 +762,10 @@ __device__ void softmax_unit(const GroupArgs& ga, Smem& sm, Cursor& cur, int r0,
             l *= ex2(m_used - m_new);
             m_used = m_new;
         }
-        // ---- P(g) into shared-memory buffer buf once P V of stage g - 2 has
-        // consumed it: row = slot, 8 chunks of 8 tokens (128-byte swizzle)
-        if (g >= 2)
-            wait_or_abort(sm, &sm.p_free[buf], ((g >> 1) - 1) & 1);
-        // every column unconditionally (masked ones give 0): straight-line
-        // code lets the exponentials of all 64 columns overlap
+        // ---- P(g) into the first 32 columns of the stage's score buffer (its
+        // scores are in registers; Q K^T of stage g waited for P V of stage
+        // g - 2, the buffer's previous user): every column unconditionally
+        // (masked ones give 0), straight-line so the exponentials overlap
         const float m_off = m_new == -INFINITY ? 0.f : -m_new;
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
         uint32_t pk[32];
@@ -738,13 +777,10 @@ __device__ void softmax_unit(const GroupArgs& ga, Smem& sm, Cursor& cur, int r0,
             pk[c] = pack_half2(p0, p1);
         }
         l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-        unsigned char* prow = sm.p[buf] + slot * 128;
-#pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8)
-            *reinterpret_cast<uint4*>(prow + ((c8 ^ (slot & 7)) << 4)) =
-                make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
-        if (dup)                               // duplicated selections: count per listing
-            l += scale_listed(a, sm, prow, slot, r0 + rl, own, nbw, kStageBlocks * i, live16);
+        tc::tmem_st32(tl + kTmemS + 64 * buf, pk);
+        if (__any_sync(0xffffffffu, dup))      // duplicated selections: count per listing
+            l += scale_listed(a, sm, tl + kTmemS + 64 * buf, dup, r0 + rl, own, nbw,
+                              kStageBlocks * i, live16);
         const bool resc = m_new != m_prev && m_prev != -INFINITY;
         const bool any_resc = __any_sync(0xffffffffu, resc);
         if (any_resc) {
@@ -767,9 +803,7 @@ __device__ void softmax_unit(const GroupArgs& ga, Smem& sm, Cursor& cur, int r0,
             }
         }
 
-        tc::fence_async_shared();
-        if (any_resc)
-            tc::tmem_wait_st();                // the O rescale stores
+        tc::tmem_wait_st();                    // P and any O rescale stores
         tc::fence_before_sync();
         tc::mbar_arrive(&sm.p_full[buf]);
     }
@@ -840,13 +874,14 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_prefill_grouped_kernel(con
         }
         for (int b = 0; b < 2; ++b) {
             tc::mbar_init(&sm.s_full[b], 1);
-            tc::mbar_init(&sm.s_free[b], kGroupThreads);   // one warpgroup reads S(g)
             tc::mbar_init(&sm.p_full[b], kGroupThreads);   // and writes P(g)
             tc::mbar_init(&sm.p_free[b], 1);
         }
         tc::mbar_init(&sm.done, 3);                         // all three MMA issuers commit
-        for (int s = 0; s < kNS; ++s)
+        for (int s = 0; s < kNS; ++s) {
             sm.taken[0][s] = sm.taken[1][s] = sm.taken[2][s] = 0u;
+            sm.slot_pub[s] = 0u;
+        }
         sm.abort = 0;
         sm.spin_limit = ga.spin_limit > 0 ? ga.spin_limit : tc::kSpinLimit;
         tc::mbar_init_fence();
