@@ -380,17 +380,15 @@ int paged_gqa_sparse_prefill_group_rows(int R, int Hq, int Hkv, int rows_per_gro
         return PAGED_GQA_ERR_UNSUPPORTED;
     if (rows_per_group > kGroupSlots / (Hq / Hkv))
         return PAGED_GQA_ERR_SHAPE;
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        sms <= 0)
+    int clusters = 0;
+    if (grouped_prefill_clusters(clusters) != cudaSuccess || clusters <= 0)
         return PAGED_GQA_ERR_CUDA;
     PrefillArgs a{};
     a.R = R;
     a.Hq = Hq;
     a.Hkv = Hkv;
     a.G = Hq / Hkv;
-    return grouped_prefill_rows(a, sms, rows_per_group);
+    return grouped_prefill_rows(a, clusters, rows_per_group);
 }
 
 int paged_gqa_gather_dequant(const void* cache, paged_gqa_kv_layout kv_layout, int kv_dtype,

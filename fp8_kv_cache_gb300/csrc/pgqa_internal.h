@@ -109,7 +109,8 @@ int split_ctas_per_sm(bool e4m3);
 cudaError_t launch_decode(const DecodeArgs& a, bool e4m3, cudaStream_t s, void* ev0, void* ev1);
 cudaError_t launch_prefill(const PrefillArgs& a, bool e4m3, cudaStream_t s);
 bool grouped_prefill_supported(const PrefillArgs& a);
-int grouped_prefill_rows(const PrefillArgs& a, int sms, int rows_per_group);
+int grouped_prefill_rows(const PrefillArgs& a, int clusters, int rows_per_group);
+cudaError_t grouped_prefill_clusters(int& clusters);
 cudaError_t launch_prefill_grouped(const PrefillArgs& a, bool e4m3, int rows_per_group,
                                    cudaStream_t s, long spin_limit = 0, int stall_stage = -1);
 cudaError_t launch_gather(const KVGeom& g, bool e4m3, const int32_t* bt, int64_t bt_stride,

@@ -89,6 +89,7 @@ struct Smem {
     int row_p[kM], row_own[kM], row_rank_own[kM], row_dup[kM];
     float mref[kM];                          // [slot]: reference maximum handed between the groups
     float xl[2][kM];                         // [group][slot]: final sums exchanged
+    float xml[kM][2];                        // [slot]: the partner CTA's final reference and sum
     // K stage loaded (by the parity of its half-tile in the unit), V stage
     // loaded, slot free.
     uint64_t full_k[2][kNS], full_v[kNS], empty[kNS];
@@ -242,7 +243,7 @@ __device__ void build_masks(const GroupArgs& ga, Smem& sm, int r0, int Rg, int h
 // Everything a unit needs before its first stage: row positions, the union
 // bitmap and its ranks, the Q tile, the first window of masks.  All threads.
 __device__ void unit_setup(const GroupArgs& ga, Smem& sm, int r0, int Rg, int j, int nbw,
-                           int words_per_row, int cap)
+                           int words_per_row, int cap, uint32_t crank)
 {
     const PrefillArgs& a = ga.a;
     const int tid = threadIdx.x;
@@ -337,7 +338,8 @@ __device__ void unit_setup(const GroupArgs& ga, Smem& sm, int r0, int Rg, int j,
             tc::tmem_st32(tl + kTmemQ + 64 * half + 32 * part, w);
         }
         tc::tmem_wait_st();
-        build_masks(ga, sm, r0, Rg, 0, cap, words_per_row);
+        const int nt = (sm.n_union + kStageBlocks - 1) / kStageBlocks;
+        build_masks(ga, sm, r0, Rg, crank ? nt / 2 : 0, cap, words_per_row);
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -404,7 +406,7 @@ __device__ __forceinline__ int64_t stage_block_offset(const GroupArgs& ga, const
 // barrier of its kind; stages of different warps are in flight together.
 template <bool kE4M3>
 __device__ void produce(const GroupArgs& ga, Smem& sm, Cursor& cur, int j, int nbw, int nt,
-                        int n_union)
+                        int h0, int n_union)
 {
     const PrefillArgs& a = ga.a;
     const int lane = threadIdx.x & 31, pw = (threadIdx.x >> 5) - kProdWarp0;
@@ -416,7 +418,7 @@ __device__ void produce(const GroupArgs& ga, Smem& sm, Cursor& cur, int j, int n
     int64_t off = -1;
     if (q < n) {
         stage_of(q, nt, is_v, ht);
-        off = stage_block_offset(ga, sm, j, nbw, n_union, ht, lane);
+        off = stage_block_offset(ga, sm, j, nbw, n_union, h0 + ht, lane);
     }
     for (; q < n; q += kProdWarps) {
         const uint32_t it = it0 + q;
@@ -452,7 +454,7 @@ __device__ void produce(const GroupArgs& ga, Smem& sm, Cursor& cur, int j, int n
             }
             cp_async_commit();
             if (qn < n)                          // the next stage's rows, while these copies fly
-                off_next = stage_block_offset(ga, sm, j, nbw, n_union, nh, lane);
+                off_next = stage_block_offset(ga, sm, j, nbw, n_union, h0 + nh, lane);
             cp_async_wait<0>();
             __syncwarp();
             // codes 128..255 of every row into registers (chunk idx = lane +
@@ -515,7 +517,7 @@ __device__ void produce(const GroupArgs& ga, Smem& sm, Cursor& cur, int j, int n
             }
             cp_async_commit();
             if (qn < n)                          // the next stage's rows, while these copies fly
-                off_next = stage_block_offset(ga, sm, j, nbw, n_union, nh, lane);
+                off_next = stage_block_offset(ga, sm, j, nbw, n_union, h0 + nh, lane);
             cp_async_wait<0>();
         }
         tc::fence_async_shared();
@@ -681,12 +683,12 @@ __device__ __forceinline__ void named_arrive(int id)
 // was folded into Q), so a masked score of -inf gives P = 0 directly.
 // At the end of the unit both groups bring their sums to the final reference,
 // add them, and split the output columns (group wg writes 128 wg ... + 127).
-__device__ void softmax_unit(const GroupArgs& ga, Smem& sm, Cursor& cur, int r0, int Rg, int j,
-                             int nt, int nbw, int cap, int words_per_row, float sl2)
+__device__ float2 softmax_unit(const GroupArgs& ga, Smem& sm, Cursor& cur, int r0, int Rg,
+                               int nt, int h0, int nbw, int cap, int words_per_row, float sl2)
 {
     const PrefillArgs& a = ga.a;
     const int t = threadIdx.x, wg = t >> 7, slot = t & (kM - 1), wq = (t >> 5) & 3;
-    const int rl = slot / a.G, h = slot - rl * a.G;
+    const int rl = slot / a.G;
     const bool slot_ok = rl < Rg;
     const int own = slot_ok ? sm.row_own[rl] : -1;
     const int rank_own = slot_ok ? sm.row_rank_own[rl] : -1;
@@ -703,7 +705,7 @@ __device__ void softmax_unit(const GroupArgs& ga, Smem& sm, Cursor& cur, int r0,
         const int wi = i / cap;
         while (win < wi) {                     // both groups rebuild every window once
             ++win;
-            build_masks(ga, sm, r0, Rg, win * cap, cap, words_per_row);
+            build_masks(ga, sm, r0, Rg, h0 + win * cap, cap, words_per_row);
         }
         uint32_t live16 = 0u;                  // blocks of the stage the slot attends
         if (own >= 0) {
@@ -726,7 +728,7 @@ __device__ void softmax_unit(const GroupArgs& ga, Smem& sm, Cursor& cur, int r0,
             for (int u = 0; u < 4; ++u)
                 x[4 * kb + u] = pb ? __uint_as_float(sv[4 * kb + u]) : -INFINITY;
         }
-        if (rank_own >= 0 && (rank_own >> 4) == i) {   // the row's own block: tokens <= p
+        if (rank_own >= 0 && (rank_own >> 4) == h0 + i) {   // the row's own block: tokens <= p
             const int ko = rank_own & 15;
 #pragma unroll
             for (int kb = 0; kb < kStageBlocks; ++kb)
@@ -780,7 +782,7 @@ __device__ void softmax_unit(const GroupArgs& ga, Smem& sm, Cursor& cur, int r0,
         tc::tmem_st32(tl + kTmemS + 64 * buf, pk);
         if (__any_sync(0xffffffffu, dup))      // duplicated selections: count per listing
             l += scale_listed(a, sm, tl + kTmemS + 64 * buf, dup, r0 + rl, own, nbw,
-                              kStageBlocks * i, live16);
+                              kStageBlocks * (h0 + i), live16);
         const bool resc = m_new != m_prev && m_prev != -INFINITY;
         const bool any_resc = __any_sync(0xffffffffu, resc);
         if (any_resc) {
@@ -812,7 +814,7 @@ __device__ void softmax_unit(const GroupArgs& ga, Smem& sm, Cursor& cur, int r0,
     const int last_win = nt > 0 ? (nt - 1) / cap : 0;
     while (win < last_win) {                   // rebuilds the other group still makes
         ++win;
-        build_masks(ga, sm, r0, Rg, win * cap, cap, words_per_row);
+        build_masks(ga, sm, r0, Rg, h0 + win * cap, cap, words_per_row);
     }
     float m_fin = m_used;
     if (nt > 0 && wg != ((nt - 1) & 1)) {      // the other group ran the last stage
@@ -829,32 +831,103 @@ __device__ void softmax_unit(const GroupArgs& ga, Smem& sm, Cursor& cur, int r0,
         wait_or_abort(sm, &sm.p_free[g_last & 1], (g_last >> 1) & 1);
         tc::fence_after_sync();
     }
-    const float inv = lt > 0.f ? a.v_scale / lt : 0.f;     // E4M3: the per-tensor scale of V
-    uint4* dst = slot_ok ? reinterpret_cast<uint4*>(
-                               a.out + ((size_t)(r0 + rl) * a.Hq + (size_t)j * a.G + h) * kD +
-                               128 * wg)
+    tc::fence_before_sync();
+    cur.g = g0 + nt;
+    return make_float2(nt > 0 ? m_fin : -INFINITY, nt > 0 ? lt : 0.f);
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Barrier of every thread of both CTAs of the cluster; the writes before it
+// (shared memory of either CTA) are visible after it.
+__device__ __forceinline__ void cluster_sync_all()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// The two CTAs of a cluster each ran half of a unit's stages (rank 0 the
+// first half) into their own TMEM accumulators, each with its own final
+// reference m and sum l per slot.  CTA rank c writes output dimensions
+// 128 c .. 128 c + 127; each softmax thread (slot, warpgroup wg) owns 64 of
+// them.  Step 1 (between the two cluster barriers): send the partner the
+// thread's accumulator over the partner's 64 dimensions, and (wg 0) m and l,
+// into the partner's shared memory (the first two ring slots: the ring is
+// idle between units).  Step 2: combine the two halves,
+//   out = (2^(m_a - M) O_a + 2^(m_b - M) O_b) / (2^(m_a - M) l_a + 2^(m_b - M) l_b)
+// (M = max(m_a, m_b); a half with l = 0 adds nothing), and write FP16.
+__device__ void pair_send(Smem& sm, uint32_t crank, float2 ml)
+{
+    const int t = threadIdx.x, wg = t >> 7, slot = t & (kM - 1), wq = (t >> 5) & 3;
+    const uint32_t tl = sm.tmem_base + ((uint32_t)(32 * wq) << 16);
+    const uint32_t peer = crank ^ 1u;
+    float* xb = reinterpret_cast<float*>(sm.ring[0]) + slot * 128 + 64 * wg;
+    uint32_t rb;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(tc::smem_addr(xb)), "r"(peer));
+    const bool have = ml.y > 0.f;
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+        uint32_t o[16];
+        tc::tmem_ld16(tl + kTmemO + 128 * peer + 64 * wg + 16 * c, o);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            asm volatile("st.shared::cluster.v4.u32 [%0], {%1,%2,%3,%4};"
+                         ::"r"(rb + 64 * c + 16 * e), "r"(have ? o[4 * e] : 0u),
+                         "r"(have ? o[4 * e + 1] : 0u), "r"(have ? o[4 * e + 2] : 0u),
+                         "r"(have ? o[4 * e + 3] : 0u) : "memory");
+    }
+    if (wg == 0) {
+        uint32_t rm;
+        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rm) : "r"(tc::smem_addr(&sm.xml[slot][0])), "r"(peer));
+        asm volatile("st.shared::cluster.v2.f32 [%0], {%1,%2};" ::"r"(rm), "f"(ml.x), "f"(ml.y) : "memory");
+    }
+}
+
+__device__ void pair_combine(const GroupArgs& ga, Smem& sm, int r0, int Rg, int j, uint32_t crank,
+                             float2 ml)
+{
+    const PrefillArgs& a = ga.a;
+    const int t = threadIdx.x, wg = t >> 7, slot = t & (kM - 1), wq = (t >> 5) & 3;
+    const int rl = slot / a.G, h = slot - rl * a.G;
+    const uint32_t tl = sm.tmem_base + ((uint32_t)(32 * wq) << 16);
+    const float m_a = ml.x, l_a = ml.y, m_b = sm.xml[slot][0], l_b = sm.xml[slot][1];
+    const float M = fmaxf(m_a, m_b);
+    const float w_a = l_a > 0.f ? ex2(m_a - M) : 0.f, w_b = l_b > 0.f ? ex2(m_b - M) : 0.f;
+    const float den = w_a * l_a + w_b * l_b;
+    const float inv = den > 0.f ? a.v_scale / den : 0.f;     // E4M3: the per-tensor scale of V
+    const float* xb = reinterpret_cast<const float*>(sm.ring[0]) + slot * 128 + 64 * wg;
+    uint4* dst = rl < Rg ? reinterpret_cast<uint4*>(a.out + ((size_t)(r0 + rl) * a.Hq +
+                                                             (size_t)j * a.G + h) * kD +
+                                                    128 * crank + 64 * wg)
                          : nullptr;
 #pragma unroll 1
-    for (int c = 0; c < kD / 32; ++c) {
+    for (int c = 0; c < 4; ++c) {
         uint32_t o[16];
-        if (nt > 0) {
-            tc::tmem_ld16(tl + kTmemO + 128 * wg + 16 * c, o);
-            tc::tmem_wait_ld();
-        }
+        tc::tmem_ld16(tl + kTmemO + 128 * crank + 64 * wg + 16 * c, o);
+        tc::tmem_wait_ld();
         if (dst != nullptr) {
             uint32_t hv[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                const float v0 = (nt > 0 && lt > 0.f) ? __uint_as_float(o[2 * e]) * inv : 0.f;
-                const float v1 = (nt > 0 && lt > 0.f) ? __uint_as_float(o[2 * e + 1]) * inv : 0.f;
-                hv[e] = pack_half2(v0, v1);
+                float v[2];
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const float oa = l_a > 0.f ? __uint_as_float(o[2 * e + k]) * w_a : 0.f;
+                    const float ob = l_b > 0.f ? xb[16 * c + 2 * e + k] * w_b : 0.f;
+                    v[k] = (oa + ob) * inv;
+                }
+                hv[e] = pack_half2(v[0], v[1]);
             }
             dst[2 * c] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
             dst[2 * c + 1] = make_uint4(hv[4], hv[5], hv[6], hv[7]);
         }
     }
-    tc::fence_before_sync();
-    cur.g = g0 + nt;
 }
 
 template <bool kE4M3>
@@ -893,18 +966,24 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_prefill_grouped_kernel(con
     tc::fence_after_sync();
 
     Cursor cur;
-    const int C = gridDim.x;
+    // Clusters of two CTAs: both take the same unit, rank 0 the first half of
+    // its half-tiles, rank 1 the rest; units go to the clusters in snake order.
+    const uint32_t crank = cluster_ctarank();
+    const int C = gridDim.x / 2, ci = (int)blockIdx.x / 2;
     for (int wave = 0; wave * C < ga.n_units; ++wave) {
-        const int u = wave * C + ((wave & 1) ? C - 1 - (int)blockIdx.x : (int)blockIdx.x);
+        const int u = wave * C + ((wave & 1) ? C - 1 - ci : ci);
         if (u >= ga.n_units)
-            continue;
+            continue;                            // both CTAs of the cluster alike
         const int gi = u / a.Hkv, j = u - gi * a.Hkv;
         const int r0 = gi * ga.Rg, Rg = min(ga.Rg, a.R - r0);
         const int words_per_row = kMaskWords / Rg, cap = 2 * words_per_row;
-        unit_setup(ga, sm, r0, Rg, j, ga.nbw, words_per_row, cap);
-        const int nt = (sm.n_union + kStageBlocks - 1) / kStageBlocks;
+        unit_setup(ga, sm, r0, Rg, j, ga.nbw, words_per_row, cap, crank);
+        const int nt_all = (sm.n_union + kStageBlocks - 1) / kStageBlocks;
+        const int h0 = crank ? nt_all / 2 : 0;
+        const int nt = crank ? nt_all - nt_all / 2 : nt_all / 2;
+        float2 ml = make_float2(-INFINITY, 0.f);
         if (w >= kProdWarp0 && w < kProdWarp0 + kProdWarps)
-            produce<kE4M3>(ga, sm, cur, j, ga.nbw, nt, sm.n_union);
+            produce<kE4M3>(ga, sm, cur, j, ga.nbw, nt, h0, sm.n_union);
         else if (w == kMmaWarp && lane == 0)
             issue_qk(sm, cur, nt, 0);
         else if (w == kQkWarp1 && lane == 0)
@@ -912,12 +991,22 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_prefill_grouped_kernel(con
         else if (w == kPvWarp && lane == 0)
             issue_pv(sm, cur, nt);
         else if (w < kSoftWarps)
-            softmax_unit(ga, sm, cur, r0, Rg, j, nt, ga.nbw, cap, words_per_row,
-                         a.scale_log2 == 0.f ? 1.f : fabsf(a.scale_log2));
+            ml = softmax_unit(ga, sm, cur, r0, Rg, nt, h0, ga.nbw, cap, words_per_row,
+                              a.scale_log2 == 0.f ? 1.f : fabsf(a.scale_log2));
         if (tid == 0 && sm.flags)
             raise_flag(a.err, sm.flags);
         tc::fence_before_sync();
         __syncthreads();
+        tc::fence_after_sync();
+        // ---- the two halves: exchange across the cluster, combine, write
+        cluster_sync_all();                      // both rings idle, both accumulators final
+        if (w < kSoftWarps)
+            pair_send(sm, crank, ml);
+        cluster_sync_all();
+        if (w < kSoftWarps)
+            pair_combine(ga, sm, r0, Rg, j, crank, ml);
+        tc::fence_before_sync();
+        __syncthreads();                         // the exchange buffer and TMEM read
         tc::fence_after_sync();
     }
     if ((w == kMmaWarp || w == kPvWarp || w == kQkWarp1) && lane == 0)
@@ -945,62 +1034,99 @@ bool grouped_prefill_supported(const PrefillArgs& a)
            (int64_t)a.kv_len <= (int64_t)4 * 32 * kGroupMaxWords;
 }
 
-int grouped_prefill_rows(const PrefillArgs& a, int sms, int rows_per_group)
+int grouped_prefill_rows(const PrefillArgs& a, int clusters, int rows_per_group)
 {
     const int rg_max = grp::kM / a.G;
     if (rows_per_group > 0)
         return min(rows_per_group, rg_max);
-    // Fill whole waves of one CTA per SM with units as large as that allows.
+    // Fill whole waves of co-resident CTA pairs with units as large as that
+    // allows.
     const int64_t units_min = (int64_t)((a.R + rg_max - 1) / rg_max) * a.Hkv;
-    const int64_t waves = (units_min + sms - 1) / sms;
-    const int64_t groups = std::max<int64_t>(1, waves * sms / a.Hkv);
+    const int64_t waves = (units_min + clusters - 1) / clusters;
+    const int64_t groups = std::max<int64_t>(1, waves * clusters / a.Hkv);
     return (int)std::min<int64_t>(rg_max, (a.R + groups - 1) / groups);
 }
 
-cudaError_t launch_prefill_grouped(const PrefillArgs& a, bool e4m3, int rows_per_group,
-                                   cudaStream_t s, long spin_limit, int stall_stage)
+namespace {
+
+// The kernel's launch shape: clusters of two CTAs, one CTA per SM.
+cudaLaunchConfig_t grouped_config(int clusters, cudaStream_t s, cudaLaunchAttribute* attr)
 {
-    static std::atomic<int> attr_done[2][kMaxDevices];
-    static std::atomic<int> sm_count[kMaxDevices];
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(2 * clusters));
+    cfg.blockDim = dim3(grp::kThreads);
+    cfg.dynamicSmemBytes = grp::kSmemBytes;
+    cfg.stream = s;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cfg;
+}
+
+}  // namespace
+
+// CTA pairs of the grouped kernel that the current device holds at once
+// (cached per device; the kernels' shared-memory attribute is set here).
+cudaError_t grouped_prefill_clusters(int& clusters)
+{
+    static std::atomic<int> cached[kMaxDevices];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
     if (dev < 0 || dev >= kMaxDevices)
         return cudaErrorInvalidDevice;
-    int sms = sm_count[dev].load(std::memory_order_acquire);
-    if (sms == 0) {
-        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    clusters = cached[dev].load(std::memory_order_acquire);
+    if (clusters > 0)
+        return cudaSuccess;
+    for (int k = 0; k < 2; ++k) {
+        e = k ? cudaFuncSetAttribute(grp::sparse_prefill_grouped_kernel<true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)grp::kSmemBytes)
+              : cudaFuncSetAttribute(grp::sparse_prefill_grouped_kernel<false>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)grp::kSmemBytes);
         if (e != cudaSuccess)
             return e;
-        sm_count[dev].store(sms, std::memory_order_release);
     }
-    if (!attr_done[e4m3][dev].load(std::memory_order_acquire)) {
-        e = e4m3 ? cudaFuncSetAttribute(grp::sparse_prefill_grouped_kernel<true>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)grp::kSmemBytes)
-                 : cudaFuncSetAttribute(grp::sparse_prefill_grouped_kernel<false>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)grp::kSmemBytes);
-        if (e != cudaSuccess)
-            return e;
-        attr_done[e4m3][dev].store(1, std::memory_order_release);
-    }
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess)
+        return e;
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = grouped_config(sms / 2, nullptr, attr);
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, grp::sparse_prefill_grouped_kernel<false>, &cfg);
+    if (e != cudaSuccess)
+        return e;
+    clusters = std::max(1, std::min(n, sms / 2));
+    cached[dev].store(clusters, std::memory_order_release);
+    return cudaSuccess;
+}
+
+cudaError_t launch_prefill_grouped(const PrefillArgs& a, bool e4m3, int rows_per_group,
+                                   cudaStream_t s, long spin_limit, int stall_stage)
+{
+    int clusters = 0;
+    cudaError_t e = grouped_prefill_clusters(clusters);
+    if (e != cudaSuccess)
+        return e;
     GroupArgs ga{};
     ga.a = a;
-    ga.Rg = grouped_prefill_rows(a, sms, rows_per_group);
+    ga.Rg = grouped_prefill_rows(a, clusters, rows_per_group);
     const int64_t groups = (a.R + ga.Rg - 1) / ga.Rg;
     ga.n_units = (int)(groups * a.Hkv);
     const int64_t blocks = a.kv_len > 0 ? ((int64_t)a.kv_len + 3) / 4 : 1;
     ga.nbw = (int)std::max<int64_t>(1, (blocks + 31) / 32);
     ga.spin_limit = spin_limit;
     ga.stall_stage = stall_stage;
-    const int grid = std::min(ga.n_units, sms);
-    if (e4m3)
-        grp::sparse_prefill_grouped_kernel<true><<<grid, grp::kThreads, grp::kSmemBytes, s>>>(ga);
-    else
-        grp::sparse_prefill_grouped_kernel<false><<<grid, grp::kThreads, grp::kSmemBytes, s>>>(ga);
-    return cudaGetLastError();
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = grouped_config(std::min(ga.n_units, clusters), s, attr);
+    return e4m3 ? cudaLaunchKernelEx(&cfg, grp::sparse_prefill_grouped_kernel<true>, ga)
+                : cudaLaunchKernelEx(&cfg, grp::sparse_prefill_grouped_kernel<false>, ga);
 }
 
 }  // namespace pgqa
