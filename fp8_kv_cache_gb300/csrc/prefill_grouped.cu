@@ -190,6 +190,25 @@ __device__ __forceinline__ int entry_block(const GroupArgs& ga, const Smem& sm, 
     return b;
 }
 
+// entry_block for a unit whose union bitmap is built: a block whose page is
+// invalid never entered the union (its flag was raised then), so the
+// bitmap stands in for the page-table check.
+__device__ __forceinline__ int entry_block_in_union(const GroupArgs& ga, const Smem& sm, int r0,
+                                                    int rl, int e)
+{
+    const PrefillArgs& a = ga.a;
+    const int own = sm.row_own[rl];
+    if (own < 0)
+        return -1;
+    int b = own;
+    if (e < a.n_sel) {
+        b = __ldg(a.sel + (size_t)(r0 + rl) * a.n_sel + e);
+        if (b < 0 || b >= own)
+            return -1;
+    }
+    return (sm.bitmap[b >> 5] >> (b & 31)) & 1u ? b : -1;
+}
+
 __device__ __forceinline__ int rank_of_block(const Smem& sm, int b)
 {
     const int w = b >> 5;
@@ -223,10 +242,10 @@ __device__ void build_masks(const GroupArgs& ga, Smem& sm, int r0, int Rg, int h
         sm.masks[i] = 0u;
     asm volatile("bar.sync 1, %0;" ::"n"(kSoftWarps * 32) : "memory");
     const int n_ent = ga.a.n_sel + 1;
-    int flags = 0;
+#pragma unroll 4
     for (int idx = t; idx < Rg * n_ent; idx += kSoftWarps * 32) {
         const int rl = idx / n_ent, e = idx - rl * n_ent;
-        const int b = entry_block(ga, sm, r0, rl, e, flags);
+        const int b = entry_block_in_union(ga, sm, r0, rl, e);
         if (b < 0)
             continue;
         const int k = rank_of_block(sm, b), ht = (k >> 4) - ht0;
@@ -275,6 +294,7 @@ __device__ void unit_setup(const GroupArgs& ga, Smem& sm, int r0, int Rg, int j,
 
     const int n_ent = a.n_sel + 1;
     int flags = 0;
+#pragma unroll 4
     for (int idx = tid; idx < Rg * n_ent; idx += kThreads) {
         const int rl = idx / n_ent, e = idx - rl * n_ent;
         const int b = entry_block(ga, sm, r0, rl, e, flags);
