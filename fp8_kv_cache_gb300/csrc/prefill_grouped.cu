@@ -877,18 +877,25 @@ __device__ __forceinline__ void cluster_sync_all()
 // 128 c .. 128 c + 127; each softmax thread (slot, warpgroup wg) owns 64 of
 // them.  Step 1 (between the two cluster barriers): send the partner the
 // thread's accumulator over the partner's 64 dimensions, and (wg 0) m and l,
-// into the partner's shared memory (the first two ring slots: the ring is
-// idle between units).  Step 2: combine the two halves,
+// into the partner's shared memory (the first two ring slots, swizzled: the
+// ring is idle between units).  Step 2: combine the two halves,
 //   out = (2^(m_a - M) O_a + 2^(m_b - M) O_b) / (2^(m_a - M) l_a + 2^(m_b - M) l_b)
 // (M = max(m_a, m_b); a half with l = 0 adds nothing), and write FP16.
+// Exchange buffer: slot s's 128 floats are 32 chunks of 16 bytes at
+// 512 s + 16 (c ^ (s & 7)) bytes of the first two ring slots, so the lanes of a
+// warp (consecutive slots) spread their 16-byte accesses over all banks.
+__device__ __forceinline__ uint32_t xchg_offset(int slot, int chunk)
+{
+    return (uint32_t)(512 * slot + 16 * (chunk ^ (slot & 7)));
+}
+
 __device__ void pair_send(Smem& sm, uint32_t crank, float2 ml)
 {
     const int t = threadIdx.x, wg = t >> 7, slot = t & (kM - 1), wq = (t >> 5) & 3;
     const uint32_t tl = sm.tmem_base + ((uint32_t)(32 * wq) << 16);
     const uint32_t peer = crank ^ 1u;
-    float* xb = reinterpret_cast<float*>(sm.ring[0]) + slot * 128 + 64 * wg;
     uint32_t rb;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(tc::smem_addr(xb)), "r"(peer));
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(tc::smem_addr(sm.ring[0])), "r"(peer));
     const bool have = ml.y > 0.f;
 #pragma unroll 1
     for (int c = 0; c < 4; ++c) {
@@ -898,9 +905,10 @@ __device__ void pair_send(Smem& sm, uint32_t crank, float2 ml)
 #pragma unroll
         for (int e = 0; e < 4; ++e)
             asm volatile("st.shared::cluster.v4.u32 [%0], {%1,%2,%3,%4};"
-                         ::"r"(rb + 64 * c + 16 * e), "r"(have ? o[4 * e] : 0u),
-                         "r"(have ? o[4 * e + 1] : 0u), "r"(have ? o[4 * e + 2] : 0u),
-                         "r"(have ? o[4 * e + 3] : 0u) : "memory");
+                         ::"r"(rb + xchg_offset(slot, 16 * wg + 4 * c + e)),
+                         "r"(have ? o[4 * e] : 0u), "r"(have ? o[4 * e + 1] : 0u),
+                         "r"(have ? o[4 * e + 2] : 0u), "r"(have ? o[4 * e + 3] : 0u)
+                         : "memory");
     }
     if (wg == 0) {
         uint32_t rm;
@@ -921,7 +929,7 @@ __device__ void pair_combine(const GroupArgs& ga, Smem& sm, int r0, int Rg, int 
     const float w_a = l_a > 0.f ? ex2(m_a - M) : 0.f, w_b = l_b > 0.f ? ex2(m_b - M) : 0.f;
     const float den = w_a * l_a + w_b * l_b;
     const float inv = den > 0.f ? a.v_scale / den : 0.f;     // E4M3: the per-tensor scale of V
-    const float* xb = reinterpret_cast<const float*>(sm.ring[0]) + slot * 128 + 64 * wg;
+    const unsigned char* xb = sm.ring[0];
     uint4* dst = rl < Rg ? reinterpret_cast<uint4*>(a.out + ((size_t)(r0 + rl) * a.Hq +
                                                              (size_t)j * a.G + h) * kD +
                                                     128 * crank + 64 * wg)
@@ -930,6 +938,15 @@ __device__ void pair_combine(const GroupArgs& ga, Smem& sm, int r0, int Rg, int 
     for (int c = 0; c < 4; ++c) {
         uint32_t o[16];
         tc::tmem_ld16(tl + kTmemO + 128 * crank + 64 * wg + 16 * c, o);
+        float pb[16];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float4 v = *reinterpret_cast<const float4*>(xb + xchg_offset(slot, 16 * wg + 4 * c + e));
+            pb[4 * e] = v.x;
+            pb[4 * e + 1] = v.y;
+            pb[4 * e + 2] = v.z;
+            pb[4 * e + 3] = v.w;
+        }
         tc::tmem_wait_ld();
         if (dst != nullptr) {
             uint32_t hv[8];
@@ -939,7 +956,7 @@ __device__ void pair_combine(const GroupArgs& ga, Smem& sm, int r0, int Rg, int 
 #pragma unroll
                 for (int k = 0; k < 2; ++k) {
                     const float oa = l_a > 0.f ? __uint_as_float(o[2 * e + k]) * w_a : 0.f;
-                    const float ob = l_b > 0.f ? xb[16 * c + 2 * e + k] * w_b : 0.f;
+                    const float ob = l_b > 0.f ? pb[2 * e + k] * w_b : 0.f;
                     v[k] = (oa + ob) * inv;
                 }
                 hv[e] = pack_half2(v[0], v[1]);
