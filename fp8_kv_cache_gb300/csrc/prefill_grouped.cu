@@ -162,37 +162,9 @@ __device__ __forceinline__ bool page_valid_block(const KVGeom& g, const int32_t*
 }
 
 // Block of entry e of group row rl (selected blocks, then the own block), or
-// -1 when the entry is not attended; adds the entry's flags.
-__device__ __forceinline__ int entry_block(const GroupArgs& ga, const Smem& sm, int r0, int rl,
-                                           int e, int& flags)
-{
-    const PrefillArgs& a = ga.a;
-    const int own = sm.row_own[rl];
-    if (own < 0)
-        return -1;
-    int b;
-    if (e < a.n_sel) {
-        b = __ldg(a.sel + (size_t)(r0 + rl) * a.n_sel + e);
-        if (b < 0)
-            return -1;
-        if (b >= own) {
-            flags |= PAGED_GQA_FLAG_BAD_SEL;
-            return -1;
-        }
-    } else {
-        b = own;
-    }
-    int page, slot;
-    if (!page_valid_block(a.kv, a.bt, b, page, slot)) {
-        flags |= PAGED_GQA_FLAG_BAD_PAGE;
-        return -1;
-    }
-    return b;
-}
-
-// entry_block for a unit whose union bitmap is built: a block whose page is
-// invalid never entered the union (its flag was raised then), so the
-// bitmap stands in for the page-table check.
+// -1 when the entry is not attended.  Setup has built the union bitmap and
+// taken the blocks with invalid pages out of it (raising their flag then),
+// so the bitmap stands in for the page-table check.
 __device__ __forceinline__ int entry_block_in_union(const GroupArgs& ga, const Smem& sm, int r0,
                                                     int rl, int e)
 {
@@ -259,17 +231,115 @@ __device__ void build_masks(const GroupArgs& ga, Smem& sm, int r0, int Rg, int h
     asm volatile("bar.sync 1, %0;" ::"n"(kSoftWarps * 32) : "memory");
 }
 
+// Setup stages its inputs in the ring, idle between units: the Q rows of
+// the unit's slots in the first 64 KB (slot s's 32 chunks of 16 bytes at
+// 512 s + 16 (c ^ (s & 31)), so a warp reading one chunk of 32 slots is free
+// of bank conflicts), its selection entries (row-major, as in memory) after
+// them, at most kSelStage at a time.
+constexpr int kStageQBytes = kM * kD * 2;
+constexpr int kSelStage = (kNS * kStageBytes - kStageQBytes) / 4 - 4;
+
+// cp.async of entries [c0, c0 + n) of the unit's selection rows into the
+// ring; the staged copy keeps the source's offset modulo 16 bytes.  Returns
+// where entry c0 lands.
+__device__ __forceinline__ const int32_t* stage_sel(const PrefillArgs& a, Smem& sm, int r0, int c0,
+                                                    int n)
+{
+    const int32_t* src = a.sel + (size_t)r0 * a.n_sel + c0;
+    unsigned char* dst = &sm.ring[0][0] + kStageQBytes +
+                         (reinterpret_cast<uintptr_t>(src) & 15u);
+    const uint32_t d0 = tc::smem_addr(dst);
+    for (int i = threadIdx.x; i < n; i += kThreads)
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(d0 + 4u * i), "l"(src + i)
+                     : "memory");
+    return reinterpret_cast<const int32_t*>(dst);
+}
+
+// Selected entries [c0, c0 + n) of the unit, staged at st, OR-ed into the
+// union bitmap (padding and rows without a position skipped; a block at or
+// after its row's own block is flagged and skipped).
+__device__ __forceinline__ void union_entries(const PrefillArgs& a, Smem& sm, const int32_t* st,
+                                              int c0, int n, int& flags)
+{
+#pragma unroll 4
+    for (int i = threadIdx.x; i < n; i += kThreads) {
+        const int rl = (c0 + i) / a.n_sel;
+        const int own = sm.row_own[rl], b = st[i];
+        if (own < 0 || b < 0)
+            continue;
+        if (b >= own) {
+            flags |= PAGED_GQA_FLAG_BAD_SEL;
+            continue;
+        }
+        atomicOr(&sm.bitmap[b >> 5], 1u << (b & 31));
+    }
+}
+
+// Stage masks of half-tiles [ht0, ht0 + cap) from the staged entries of a
+// unit whose entries all fit in one staging (the masks are zero): the same
+// masks as build_masks, built by all threads.
+__device__ void staged_masks(const PrefillArgs& a, Smem& sm, const int32_t* st, int Rg, int ht0,
+                             int cap, int words_per_row)
+{
+    const int n_all = Rg * a.n_sel;
+#pragma unroll 4
+    for (int i = threadIdx.x; i < n_all + Rg; i += kThreads) {
+        int rl, b;
+        if (i < n_all) {
+            rl = i / a.n_sel;
+            const int own = sm.row_own[rl];
+            b = st[i];
+            if (own < 0 || b < 0 || b >= own)
+                continue;
+        } else {
+            rl = i - n_all;
+            b = sm.row_own[rl];
+            if (b < 0)
+                continue;
+        }
+        if (!((sm.bitmap[b >> 5] >> (b & 31)) & 1u))
+            continue;                            // its page is invalid
+        const int k = rank_of_block(sm, b), ht = (k >> 4) - ht0;
+        if (ht < 0 || ht >= cap)
+            continue;
+        const uint32_t bit = 1u << (((ht & 1) << 4) + (k & 15));
+        const uint32_t old = atomicOr(&sm.masks[rl * words_per_row + (ht >> 1)], bit);
+        if (old & bit)
+            sm.row_dup[rl] = 1;
+    }
+}
+
 // Everything a unit needs before its first stage: row positions, the union
 // bitmap and its ranks, the Q tile, the first window of masks.  All threads.
+// The selection entries and Q are fetched by cp.async in one round trip; the
+// page of each union block is checked once (an invalid one leaves the union
+// and raises PAGED_GQA_FLAG_BAD_PAGE, as it would for each of its entries).
 __device__ void unit_setup(const GroupArgs& ga, Smem& sm, int r0, int Rg, int j, int nbw,
                            int words_per_row, int cap, uint32_t crank)
 {
     const PrefillArgs& a = ga.a;
     const int tid = threadIdx.x;
+    const int n_all = Rg * a.n_sel;
+    const int n_chunks = (n_all + kSelStage - 1) / kSelStage;
     if (tid == 0) {
         sm.flags = 0;
         sm.n_union = 0;
     }
+    for (int w = tid; w < nbw; w += kThreads)
+        sm.bitmap[w] = 0u;
+    for (int i = tid; i < Rg * words_per_row; i += kThreads)
+        sm.masks[i] = 0u;
+    {                                        // Q rows: the G heads of KV head j are contiguous
+        const uint32_t q0 = tc::smem_addr(&sm.ring[0][0]);
+        for (int i = tid; i < Rg * a.G * 32; i += kThreads) {
+            const int slot = i >> 5, c = i & 31, rl = slot / a.G, h = slot - rl * a.G;
+            cp_async16(q0 + 512u * slot + 16u * (c ^ (slot & 31)),
+                       reinterpret_cast<const unsigned char*>(
+                           a.q + ((size_t)(r0 + rl) * a.Hq + (size_t)j * a.G + h) * kD + 8 * c));
+        }
+    }
+    const int32_t* st = stage_sel(a, sm, r0, 0, min(n_all, kSelStage));
+    cp_async_commit();
     if (tid < Rg) {
         int p = __ldg(a.q_pos + r0 + tid), fl = 0, own = -1;
         if (p < 0 || a.kv_len <= 0) {
@@ -288,18 +358,49 @@ __device__ void unit_setup(const GroupArgs& ga, Smem& sm, int r0, int Rg, int j,
         if (fl)
             atomicOr(&sm.flags, fl);
     }
-    for (int w = tid; w < nbw; w += kThreads)
-        sm.bitmap[w] = 0u;
+    cp_async_wait<0>();
     __syncthreads();
 
-    const int n_ent = a.n_sel + 1;
     int flags = 0;
-#pragma unroll 4
-    for (int idx = tid; idx < Rg * n_ent; idx += kThreads) {
-        const int rl = idx / n_ent, e = idx - rl * n_ent;
-        const int b = entry_block(ga, sm, r0, rl, e, flags);
-        if (b >= 0)
-            atomicOr(&sm.bitmap[b >> 5], 1u << (b & 31));
+    if (tid < Rg && sm.row_own[tid] >= 0)        // the own block
+        atomicOr(&sm.bitmap[sm.row_own[tid] >> 5], 1u << (sm.row_own[tid] & 31));
+    union_entries(a, sm, st, 0, min(n_all, kSelStage), flags);
+    for (int c = 1; c < n_chunks; ++c) {         // entries beyond one staging
+        __syncthreads();
+        const int c0 = c * kSelStage, n = min(n_all - c0, kSelStage);
+        st = stage_sel(a, sm, r0, c0, n);
+        cp_async_commit();
+        cp_async_wait<0>();
+        __syncthreads();
+        union_entries(a, sm, st, c0, n, flags);
+    }
+    __syncthreads();
+
+    {                                        // one page check per union block
+        const int nb = 32 * nbw;
+        for (int b0 = tid; b0 < nb; b0 += 8 * kThreads) {
+            int page[8];
+            uint32_t in = 0u;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int b = b0 + k * kThreads;
+                page[k] = 0;
+                if (b < nb && ((sm.bitmap[b >> 5] >> (b & 31)) & 1u)) {
+                    int pi, slot;
+                    page_and_slot(a.kv, 4 * b, pi, slot);
+                    page[k] = __ldg(a.bt + pi);
+                    in |= 1u << k;
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int b = b0 + k * kThreads;
+                if (((in >> k) & 1u) && (page[k] < 0 || page[k] >= a.kv.num_pages)) {
+                    atomicAnd(&sm.bitmap[b >> 5], ~(1u << (b & 31)));
+                    flags |= PAGED_GQA_FLAG_BAD_PAGE;
+                }
+            }
+        }
     }
     if (flags)
         atomicOr(&sm.flags, flags);
@@ -339,17 +440,18 @@ __device__ void unit_setup(const GroupArgs& ga, Smem& sm, int r0, int Rg, int j,
         const uint32_t q_xor = a.scale_log2 < 0.f ? 0x80008000u : 0u;
         const uint32_t q_and = a.scale_log2 == 0.f ? 0u : 0xFFFFFFFFu;
         const int slot = tid & (kM - 1), half = tid >> 7;         // two threads per slot
-        const int rl = slot / a.G, h = slot - rl * a.G;
+        const int rl = slot / a.G;
         const bool live = rl < Rg && sm.row_own[rl] >= 0;
-        const uint4* src = reinterpret_cast<const uint4*>(
-            a.q + ((size_t)(r0 + (live ? rl : 0)) * a.Hq + (size_t)j * a.G + (live ? h : 0)) * kD);
+        const uint32_t qs = tc::smem_addr(&sm.ring[0][0]) + 512u * slot;
         const uint32_t tl = sm.tmem_base + ((uint32_t)(32 * ((tid >> 5) & 3)) << 16);
 #pragma unroll 1
         for (int part = 0; part < 2; ++part) {   // 8 chunks of 16 bytes = 32 columns of f16 pairs
             uint32_t w[32];
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
-                const uint4 v = live ? __ldg(src + 16 * half + 8 * part + c) : make_uint4(0u, 0u, 0u, 0u);
+                const int chunk = 16 * half + 8 * part + c;
+                const uint4 v = live ? lds128(qs + 16u * (chunk ^ (slot & 31)))
+                                     : make_uint4(0u, 0u, 0u, 0u);
                 w[4 * c] = (v.x ^ q_xor) & q_and;
                 w[4 * c + 1] = (v.y ^ q_xor) & q_and;
                 w[4 * c + 2] = (v.z ^ q_xor) & q_and;
@@ -358,9 +460,13 @@ __device__ void unit_setup(const GroupArgs& ga, Smem& sm, int r0, int Rg, int j,
             tc::tmem_st32(tl + kTmemQ + 64 * half + 32 * part, w);
         }
         tc::tmem_wait_st();
-        const int nt = (sm.n_union + kStageBlocks - 1) / kStageBlocks;
-        build_masks(ga, sm, r0, Rg, crank ? nt / 2 : 0, cap, words_per_row);
     }
+    const int nt = (sm.n_union + kStageBlocks - 1) / kStageBlocks;
+    const int ht0 = crank ? nt / 2 : 0;
+    if (n_chunks <= 1)
+        staged_masks(a, sm, st, Rg, ht0, cap, words_per_row);
+    else if (tid < kSoftWarps * 32)
+        build_masks(ga, sm, r0, Rg, ht0, cap, words_per_row);
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
