@@ -106,7 +106,9 @@ struct Smem {
     // which keeps the slot's empty barrier at most one phase behind the
     // parity this producer waits for.
     uint32_t slot_pub[kNS];
-    uint64_t s_full[2], p_full[2], p_free[2], done;
+    // S written; P's first 32 tokens written (p_half) and all of P (p_full);
+    // P V done reading P.
+    uint64_t s_full[2], p_half[2], p_full[2], p_free[2], done;
     uint32_t tmem_base;
     int flags, n_union, abort;
     long spin_limit;
@@ -712,16 +714,20 @@ __device__ void issue_pv(Smem& sm, Cursor& cur, int nt)
         const uint32_t g = g0 + ht, buf = g & 1, s = cur.it % kNS;
         const uint32_t st = tc::smem_addr(sm.ring[s]);
         wait_or_abort(sm, &sm.full_v[s], sm.taken[2][s]++ & 1);
-        wait_or_abort(sm, &sm.p_full[buf], (g >> 1) & 1);
-        tc::fence_after_sync();
         const uint64_t db0 = tc::sw128_desc(st, kRegionBytes, 1024);
         const uint32_t acc0 = ht > 0;
         // P (128 slots x 64 tokens, f16 pairs) from the first 32 columns of
-        // the stage's score buffer; 16 tokens per K step = 8 columns
+        // the stage's score buffer; 16 tokens per K step = 8 columns.  The
+        // first two K steps go as soon as their half of P is written.
 #pragma unroll
-        for (int kk = 0; kk < kStageTokens / 16; ++kk)
-            tc::mma_ts(tm + kTmemO, tm + kTmemS + 64 * buf + 8 * kk,
-                       db0 + (uint64_t)(kk * 128), kIdPV, kk > 0 ? 1u : acc0);
+        for (int half = 0; half < 2; ++half) {
+            wait_or_abort(sm, half ? &sm.p_full[buf] : &sm.p_half[buf], (g >> 1) & 1);
+            tc::fence_after_sync();
+#pragma unroll
+            for (int kk = 2 * half; kk < 2 * half + 2; ++kk)
+                tc::mma_ts(tm + kTmemO, tm + kTmemS + 64 * buf + 8 * kk,
+                           db0 + (uint64_t)(kk * 128), kIdPV, kk > 0 ? 1u : acc0);
+        }
         tc::mma_commit(&sm.empty[s]);
         tc::mma_commit(&sm.p_free[buf]);
     }
@@ -890,49 +896,63 @@ __device__ float2 softmax_unit(const GroupArgs& ga, Smem& sm, Cursor& cur, int r
             l *= ex2(m_used - m_new);
             m_used = m_new;
         }
-        // ---- P(g) into the first 32 columns of the stage's score buffer (its
-        // scores are in registers; Q K^T of stage g waited for P V of stage
-        // g - 2, the buffer's previous user): every column unconditionally
-        // (masked ones give 0), straight-line so the exponentials overlap
-        const float m_off = m_new == -INFINITY ? 0.f : -m_new;
-        float ls[4] = {0.f, 0.f, 0.f, 0.f};
-        uint32_t pk[32];
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-            const float p0 = ex2(fmaf(x[2 * c], sl2, m_off));
-            const float p1 = ex2(fmaf(x[2 * c + 1], sl2, m_off));
-            ls[c & 3] += p0 + p1;
-            pk[c] = pack_half2(p0, p1);
-        }
-        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-        tc::tmem_st32(tl + kTmemS + 64 * buf, pk);
-        if (__any_sync(0xffffffffu, dup))      // duplicated selections: count per listing
-            l += scale_listed(a, sm, tl + kTmemS + 64 * buf, dup, r0 + rl, own, nbw,
-                              kStageBlocks * (h0 + i), live16);
+        // ---- a grown reference: O holds stages < i under m_prev once P V of
+        // stage i - 1 is done (P V completes in issue order); scale the
+        // lane's O row in place before any of P(g) is published (P V of
+        // stage g adds to the scaled O)
         const bool resc = m_new != m_prev && m_prev != -INFINITY;
-        const bool any_resc = __any_sync(0xffffffffu, resc);
-        if (any_resc) {
-            // O holds stages < i under m_prev once P V of stage i - 1 is done
-            // (P V completes in issue order); scale the lane's O row in place
-            // before P(g) is published (P V of stage g adds to the scaled O).
+        if (__any_sync(0xffffffffu, resc)) {
             wait_or_abort(sm, &sm.p_free[(g - 1) & 1], ((g - 1) >> 1) & 1);
             tc::fence_after_sync();
             const float f = resc ? ex2(m_prev - m_new) : 1.f;
 #pragma unroll 1
-            for (int c = 0; c < kD / 32; ++c) {
-                uint32_t o[32];
-                const uint32_t col = kTmemO + 32 * c;
-                tc::tmem_ld32(tl + col, o);
+            for (int c = 0; c < kD / 16; ++c) {    // 16 columns a step: the scores stay in registers
+                uint32_t o[16];
+                const uint32_t col = kTmemO + 16 * c;
+                tc::tmem_ld16(tl + col, o);
                 tc::tmem_wait_ld();
 #pragma unroll
-                for (int e = 0; e < 32; ++e)
+                for (int e = 0; e < 16; ++e)
                     o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
-                tc::tmem_st32(tl + col, o);
+                tc::tmem_st16(tl + col, o);
             }
         }
+        // ---- P(g) into the first 32 columns of the stage's score buffer (its
+        // scores are in registers; Q K^T of stage g waited for P V of stage
+        // g - 2, the buffer's previous user): every column unconditionally
+        // (masked ones give 0), straight-line so the exponentials overlap.
+        // The first 32 tokens are published on their own, so P V starts on
+        // them while the rest are computed; a warp with duplicated
+        // selections rescales P in place first and publishes both at the end.
+        const float m_off = m_new == -INFINITY ? 0.f : -m_new;
+        const bool wdup = __any_sync(0xffffffffu, dup);
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+                const float p0 = ex2(fmaf(x[32 * half + 2 * c], sl2, m_off));
+                const float p1 = ex2(fmaf(x[32 * half + 2 * c + 1], sl2, m_off));
+                ls[c & 3] += p0 + p1;
+                pk[c] = pack_half2(p0, p1);
+            }
+            tc::tmem_st16(tl + kTmemS + 64 * buf + 16 * half, pk);
+            if (half == 0 && !wdup) {
+                tc::tmem_wait_st();
+                tc::fence_before_sync();
+                tc::mbar_arrive(&sm.p_half[buf]);
+            }
+        }
+        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        if (wdup)                              // duplicated selections: count per listing
+            l += scale_listed(a, sm, tl + kTmemS + 64 * buf, dup, r0 + rl, own, nbw,
+                              kStageBlocks * (h0 + i), live16);
 
         tc::tmem_wait_st();                    // P and any O rescale stores
         tc::fence_before_sync();
+        if (wdup)
+            tc::mbar_arrive(&sm.p_half[buf]);
         tc::mbar_arrive(&sm.p_full[buf]);
     }
 
@@ -1003,19 +1023,18 @@ __device__ void pair_send(Smem& sm, uint32_t crank, float2 ml)
     uint32_t rb;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(tc::smem_addr(sm.ring[0])), "r"(peer));
     const bool have = ml.y > 0.f;
-#pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
-        uint32_t o[16];
-        tc::tmem_ld16(tl + kTmemO + 128 * peer + 64 * wg + 16 * c, o);
-        tc::tmem_wait_ld();
+    uint32_t o[64];                          // all 64 columns in flight at once
+    tc::tmem_ld32(tl + kTmemO + 128 * peer + 64 * wg, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
+    tc::tmem_ld32(tl + kTmemO + 128 * peer + 64 * wg + 32,
+                  *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
+    tc::tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-            asm volatile("st.shared::cluster.v4.u32 [%0], {%1,%2,%3,%4};"
-                         ::"r"(rb + xchg_offset(slot, 16 * wg + 4 * c + e)),
-                         "r"(have ? o[4 * e] : 0u), "r"(have ? o[4 * e + 1] : 0u),
-                         "r"(have ? o[4 * e + 2] : 0u), "r"(have ? o[4 * e + 3] : 0u)
-                         : "memory");
-    }
+    for (int e = 0; e < 16; ++e)
+        asm volatile("st.shared::cluster.v4.u32 [%0], {%1,%2,%3,%4};"
+                     ::"r"(rb + xchg_offset(slot, 16 * wg + e)),
+                     "r"(have ? o[4 * e] : 0u), "r"(have ? o[4 * e + 1] : 0u),
+                     "r"(have ? o[4 * e + 2] : 0u), "r"(have ? o[4 * e + 3] : 0u)
+                     : "memory");
     if (wg == 0) {
         uint32_t rm;
         asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rm) : "r"(tc::smem_addr(&sm.xml[slot][0])), "r"(peer));
@@ -1090,7 +1109,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_prefill_grouped_kernel(con
         }
         for (int b = 0; b < 2; ++b) {
             tc::mbar_init(&sm.s_full[b], 1);
-            tc::mbar_init(&sm.p_full[b], kGroupThreads);   // and writes P(g)
+            tc::mbar_init(&sm.p_half[b], kGroupThreads);   // and writes P(g)
+            tc::mbar_init(&sm.p_full[b], kGroupThreads);
             tc::mbar_init(&sm.p_free[b], 1);
         }
         tc::mbar_init(&sm.done, 3);                         // all three MMA issuers commit
