@@ -236,10 +236,13 @@ __device__ void build_masks(const GroupArgs& ga, Smem& sm, int r0, int Rg, int h
 // Setup stages its inputs in the ring, idle between units: the Q rows of
 // the unit's slots in the first 64 KB (slot s's 32 chunks of 16 bytes at
 // 512 s + 16 (c ^ (s & 31)), so a warp reading one chunk of 32 slots is free
-// of bank conflicts), its selection entries (row-major, as in memory) after
-// them, at most kSelStage at a time.
+// of bank conflicts), the sequence's block table when it has at most
+// kBtStage entries, then its selection entries (row-major, as in memory), at
+// most kSelStage at a time.
 constexpr int kStageQBytes = kM * kD * 2;
-constexpr int kSelStage = (kNS * kStageBytes - kStageQBytes) / 4 - 4;
+constexpr int kBtStage = 4096;
+constexpr int kSelOffset = kStageQBytes + 4 * kBtStage;
+constexpr int kSelStage = (kNS * kStageBytes - kSelOffset) / 4 - 4;
 
 // cp.async of entries [c0, c0 + n) of the unit's selection rows into the
 // ring; the staged copy keeps the source's offset modulo 16 bytes.  Returns
@@ -248,8 +251,7 @@ __device__ __forceinline__ const int32_t* stage_sel(const PrefillArgs& a, Smem& 
                                                     int n)
 {
     const int32_t* src = a.sel + (size_t)r0 * a.n_sel + c0;
-    unsigned char* dst = &sm.ring[0][0] + kStageQBytes +
-                         (reinterpret_cast<uintptr_t>(src) & 15u);
+    unsigned char* dst = &sm.ring[0][0] + kSelOffset + (reinterpret_cast<uintptr_t>(src) & 15u);
     const uint32_t d0 = tc::smem_addr(dst);
     for (int i = threadIdx.x; i < n; i += kThreads)
         asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(d0 + 4u * i), "l"(src + i)
@@ -257,65 +259,134 @@ __device__ __forceinline__ const int32_t* stage_sel(const PrefillArgs& a, Smem& 
     return reinterpret_cast<const int32_t*>(dst);
 }
 
+// A thread's share of entries [0, n) of the unit's selection rows, flattened
+// row-major: a contiguous run, so consecutive entries of a (usually sorted)
+// row let it gather its bitmap and mask bits per word before one atomic.
+struct EntryRun {
+    int i, i1, rl, e;
+    __device__ EntryRun(const PrefillArgs& a, int c0, int n)
+    {
+        const int per = (n + kThreads - 1) / kThreads;
+        i = min(n, (int)threadIdx.x * per);
+        i1 = min(n, i + per);
+        rl = (c0 + i) / max(a.n_sel, 1);
+        e = (c0 + i) - rl * a.n_sel;
+    }
+    __device__ void next(const PrefillArgs& a)
+    {
+        ++i;
+        if (++e == a.n_sel) {
+            e = 0;
+            ++rl;
+        }
+    }
+};
+
+// Whether block b's page is valid, from the staged block table.
+__device__ __forceinline__ bool staged_page_ok(const PrefillArgs& a, const int32_t* btab, int b)
+{
+    int pi, slot;
+    page_and_slot(a.kv, 4 * b, pi, slot);
+    const int page = btab[pi];
+    return page >= 0 && page < a.kv.num_pages;
+}
+
 // Selected entries [c0, c0 + n) of the unit, staged at st, OR-ed into the
 // union bitmap (padding and rows without a position skipped; a block at or
-// after its row's own block is flagged and skipped).
+// after its row's own block is flagged and skipped; with the block table
+// staged at btab, so is a block whose page is invalid).
 __device__ __forceinline__ void union_entries(const PrefillArgs& a, Smem& sm, const int32_t* st,
-                                              int c0, int n, int& flags)
+                                              int c0, int n, int& flags, const int32_t* btab)
 {
-#pragma unroll 4
-    for (int i = threadIdx.x; i < n; i += kThreads) {
-        const int rl = (c0 + i) / a.n_sel;
-        const int own = sm.row_own[rl], b = st[i];
-        if (own < 0 || b < 0)
-            continue;
-        if (b >= own) {
-            flags |= PAGED_GQA_FLAG_BAD_SEL;
-            continue;
+    EntryRun r(a, c0, n);
+    int cw = -1;                             // the bitmap word being gathered, its bits
+    uint32_t cb = 0u;
+    for (int own = r.i < r.i1 ? sm.row_own[r.rl] : -1; r.i < r.i1;) {
+        const int b = st[r.i];
+        if (own >= 0 && b >= 0) {
+            if (b >= own) {
+                flags |= PAGED_GQA_FLAG_BAD_SEL;
+            } else if (btab != nullptr && !staged_page_ok(a, btab, b)) {
+                flags |= PAGED_GQA_FLAG_BAD_PAGE;
+            } else {
+                if ((b >> 5) != cw) {
+                    if (cb)
+                        atomicOr(&sm.bitmap[cw], cb);
+                    cw = b >> 5;
+                    cb = 0u;
+                }
+                cb |= 1u << (b & 31);
+            }
         }
-        atomicOr(&sm.bitmap[b >> 5], 1u << (b & 31));
+        const int rl = r.rl;
+        r.next(a);
+        if (r.rl != rl && r.i < r.i1)
+            own = sm.row_own[r.rl];
     }
+    if (cb)
+        atomicOr(&sm.bitmap[cw], cb);
 }
 
 // Stage masks of half-tiles [ht0, ht0 + cap) from the staged entries of a
 // unit whose entries all fit in one staging (the masks are zero): the same
-// masks as build_masks, built by all threads.
+// masks as build_masks, built by all threads, each over a run of entries
+// with one atomic per mask word it touches.
 __device__ void staged_masks(const PrefillArgs& a, Smem& sm, const int32_t* st, int Rg, int ht0,
                              int cap, int words_per_row)
 {
     const int n_all = Rg * a.n_sel;
-#pragma unroll 4
-    for (int i = threadIdx.x; i < n_all + Rg; i += kThreads) {
-        int rl, b;
-        if (i < n_all) {
-            rl = i / a.n_sel;
-            const int own = sm.row_own[rl];
-            b = st[i];
-            if (own < 0 || b < 0 || b >= own)
-                continue;
-        } else {
-            rl = i - n_all;
-            b = sm.row_own[rl];
-            if (b < 0)
-                continue;
+    EntryRun r(a, 0, n_all);
+    int cw = -1, crl = 0;                    // the mask word being gathered, its row, its bits
+    uint32_t cb = 0u;
+    const auto flush = [&]() {
+        if (cb) {
+            const uint32_t old = atomicOr(&sm.masks[cw], cb);
+            if (old & cb)
+                sm.row_dup[crl] = 1;
         }
-        if (!((sm.bitmap[b >> 5] >> (b & 31)) & 1u))
-            continue;                            // its page is invalid
-        const int k = rank_of_block(sm, b), ht = (k >> 4) - ht0;
-        if (ht < 0 || ht >= cap)
-            continue;
-        const uint32_t bit = 1u << (((ht & 1) << 4) + (k & 15));
-        const uint32_t old = atomicOr(&sm.masks[rl * words_per_row + (ht >> 1)], bit);
-        if (old & bit)
-            sm.row_dup[rl] = 1;
+    };
+    for (int own = r.i < r.i1 ? sm.row_own[r.rl] : -1; r.i < r.i1;) {
+        const int b = st[r.i];
+        if (own >= 0 && b >= 0 && b < own && ((sm.bitmap[b >> 5] >> (b & 31)) & 1u)) {
+            const int k = rank_of_block(sm, b), ht = (k >> 4) - ht0;
+            if (ht >= 0 && ht < cap) {
+                const int wi = r.rl * words_per_row + (ht >> 1);
+                const uint32_t bit = 1u << (((ht & 1) << 4) + (k & 15));
+                if (wi != cw) {
+                    flush();
+                    cw = wi;
+                    crl = r.rl;
+                    cb = 0u;
+                }
+                if (cb & bit)                // listed twice in this run
+                    sm.row_dup[r.rl] = 1;
+                cb |= bit;
+            }
+        }
+        const int rl = r.rl;
+        r.next(a);
+        if (r.rl != rl && r.i < r.i1)
+            own = sm.row_own[r.rl];
+    }
+    flush();
+    if (threadIdx.x < Rg) {                  // the own blocks (their pages were checked)
+        const int rl = threadIdx.x, b = sm.row_own[rl];
+        if (b >= 0 && ((sm.bitmap[b >> 5] >> (b & 31)) & 1u)) {
+            const int k = rank_of_block(sm, b), ht = (k >> 4) - ht0;
+            if (ht >= 0 && ht < cap) {
+                const uint32_t bit = 1u << (((ht & 1) << 4) + (k & 15));
+                const uint32_t old = atomicOr(&sm.masks[rl * words_per_row + (ht >> 1)], bit);
+                if (old & bit)
+                    sm.row_dup[rl] = 1;
+            }
+        }
     }
 }
 
 // Everything a unit needs before its first stage: row positions, the union
 // bitmap and its ranks, the Q tile, the first window of masks.  All threads.
-// The selection entries and Q are fetched by cp.async in one round trip; the
-// page of each union block is checked once (an invalid one leaves the union
-// and raises PAGED_GQA_FLAG_BAD_PAGE, as it would for each of its entries).
+// The selection entries, Q and (when it fits) the block table are fetched by
+// cp.async in one round trip.
 __device__ void unit_setup(const GroupArgs& ga, Smem& sm, int r0, int Rg, int j, int nbw,
                            int words_per_row, int cap, uint32_t crank)
 {
@@ -341,6 +412,16 @@ __device__ void unit_setup(const GroupArgs& ga, Smem& sm, int r0, int Rg, int j,
         }
     }
     const int32_t* st = stage_sel(a, sm, r0, 0, min(n_all, kSelStage));
+    // the block table, for the page checks, when it fits
+    const int n_bt = a.kv_len > 0 ? (int)(((int64_t)a.kv_len + a.kv.page_size - 1) / a.kv.page_size) : 0;
+    const bool bt_staged = n_bt <= kBtStage;
+    const int32_t* btab = reinterpret_cast<const int32_t*>(&sm.ring[0][0] + kStageQBytes);
+    if (bt_staged) {
+        const uint32_t d0 = tc::smem_addr(&sm.ring[0][0] + kStageQBytes);
+        for (int i = tid; i < n_bt; i += kThreads)
+            asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(d0 + 4u * i), "l"(a.bt + i)
+                         : "memory");
+    }
     cp_async_commit();
     if (tid < Rg) {
         int p = __ldg(a.q_pos + r0 + tid), fl = 0, own = -1;
@@ -363,10 +444,19 @@ __device__ void unit_setup(const GroupArgs& ga, Smem& sm, int r0, int Rg, int j,
     cp_async_wait<0>();
     __syncthreads();
 
+    // The union; with the block table staged, each entry's page is checked
+    // as it joins, else each union block's page once afterwards (an invalid
+    // one leaves the union and raises BAD_PAGE, as its entries would have).
     int flags = 0;
-    if (tid < Rg && sm.row_own[tid] >= 0)        // the own block
-        atomicOr(&sm.bitmap[sm.row_own[tid] >> 5], 1u << (sm.row_own[tid] & 31));
-    union_entries(a, sm, st, 0, min(n_all, kSelStage), flags);
+    const int32_t* bt_s = bt_staged ? btab : nullptr;
+    if (tid < Rg && sm.row_own[tid] >= 0) {      // the own block
+        const int b = sm.row_own[tid];
+        if (bt_s == nullptr || staged_page_ok(a, bt_s, b))
+            atomicOr(&sm.bitmap[b >> 5], 1u << (b & 31));
+        else
+            flags |= PAGED_GQA_FLAG_BAD_PAGE;
+    }
+    union_entries(a, sm, st, 0, min(n_all, kSelStage), flags, bt_s);
     for (int c = 1; c < n_chunks; ++c) {         // entries beyond one staging
         __syncthreads();
         const int c0 = c * kSelStage, n = min(n_all - c0, kSelStage);
@@ -374,11 +464,10 @@ __device__ void unit_setup(const GroupArgs& ga, Smem& sm, int r0, int Rg, int j,
         cp_async_commit();
         cp_async_wait<0>();
         __syncthreads();
-        union_entries(a, sm, st, c0, n, flags);
+        union_entries(a, sm, st, c0, n, flags, bt_s);
     }
-    __syncthreads();
-
-    {                                        // one page check per union block
+    if (!bt_staged) {                        // one page check per union block
+        __syncthreads();
         const int nb = 32 * nbw;
         for (int b0 = tid; b0 < nb; b0 += 8 * kThreads) {
             int page[8];
