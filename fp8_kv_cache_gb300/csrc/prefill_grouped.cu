@@ -11,13 +11,17 @@
 // Design (ours, GB300-first).  The per-row kernel of prefill.cu reads each
 // row's ~2050 tokens on its own: at 4096 rows that is 8.6 GB pulled from L2
 // for a 32 MiB cache, and the gather, not the arithmetic, bounds it.  Nearby
-// rows select many of the same blocks, so here one CTA owns a group of
-// consecutive rows of one KV head -- up to 128 query-head slots, the M of one
-// tcgen05 MMA -- and streams the UNION of their blocks once:
-//   * setup: the rows' valid entries are OR-ed into a bitmap over the
-//     sequence's blocks; a prefix popcount ranks the union; each row gets a
-//     16-bit mask per 64-token stage saying which of the stage's 16 blocks it
-//     attends (its own block limited to positions <= p); Q goes to TMEM.
+// rows select many of the same blocks, so here a unit -- a group of
+// consecutive rows of one KV head, up to 128 query-head slots, the M of one
+// tcgen05 MMA -- streams the UNION of its rows' blocks once.  Persistent CTAs,
+// one per SM, run in clusters of two: both CTAs of a pair take the same unit,
+// each half of its 64-token half-tiles, and combine their results at the end.
+//   * setup: the unit's selection rows, its Q rows and (when it fits) the
+//     block table are staged in the idle ring by cp.async; the rows' valid
+//     entries are OR-ed into a bitmap over the sequence's blocks; a prefix
+//     popcount ranks the union; each row gets a 16-bit mask per 64-token
+//     stage saying which of the stage's 16 blocks it attends (its own block
+//     limited to positions <= p); Q goes to TMEM.
 //   * 5 producer warps take turns over a 6-stage ring, gathering whole
 //     stages (K and V of 64 tokens, in the order K0 K1 V0 K2 V1 ...) into the
 //     128-byte-swizzled K-major tile (see tc_device.cuh): FP16 rows by 16-byte
@@ -27,8 +31,9 @@
 //     one for the odd stages, each into its own TMEM score buffer as soon as
 //     that buffer is free, and a thread of a third warp issues O += P V
 //     (M = 128, N = 256, K = 64; P from TMEM, V from the stage bytes read as
-//     an MN-major operand) into a 256-column TMEM accumulator once a stage's
-//     probabilities are written, so Q K^T runs ahead of the softmax without
+//     an MN-major operand) into a 256-column TMEM accumulator, its first two
+//     K steps once the first half of a stage's probabilities is written and
+//     the last two once all are, so Q K^T runs ahead of the softmax without
 //     waiting behind P V.  Each issuer counts its own phases of every
 //     ring slot (K barriers per parity, a V barrier per slot), so no waiter
 //     ever runs two phases ahead of a barrier.
@@ -36,20 +41,23 @@
 //     even ones, B the odd ones), so one group's exponentials and stores
 //     overlap the other's score reads.  A thread owns one slot (its TMEM
 //     lane) and all 64 score columns of its group's stage: it reads the
-//     scores (freeing the buffer for the next Q K^T), masks them, and takes
-//     the running reference maximum from the other group's previous stage
-//     (a named-barrier handoff per lane quarter, the only link between the
-//     groups).  The reference grows only when a stage's maximum exceeds it
-//     by more than 2^8, and then O is rescaled in TMEM; each group keeps its
-//     own sum under the reference it last saw, so the result is exact up to
-//     rounding.  The FP16 probabilities go back into TMEM over the first 32
-//     columns of the stage's score buffer (its scores are in registers by
-//     then), so no shared memory holds P and the ring has a sixth slot; a
-//     score buffer is reused by Q K^T once P V has read the P in it.
+//     scores, masks them, and takes the running reference maximum from the
+//     other group's previous stage (a named-barrier handoff per lane
+//     quarter, the only link between the groups).  The reference grows only
+//     when a stage's maximum exceeds it by more than 2^8, and then O is
+//     rescaled in TMEM; each group keeps its own sum under the reference it
+//     last saw, so the result is exact up to rounding.  The FP16
+//     probabilities go back into TMEM over the first 32 columns of the
+//     stage's score buffer (its scores are in registers by then), so no
+//     shared memory holds P and the ring has a sixth slot; a score buffer is
+//     reused by Q K^T once P V has read the P in it.
+//   * the pair: each CTA sends its partner the unnormalised O of the
+//     dimensions the partner writes, with its (m, l), through distributed
+//     shared memory; each combines the two halves of its 128 dimensions.
 // Masked-out (slot, token) pairs cost tensor-core work but no memory traffic;
-// on the 4096-row workload the union is 0.60 of the per-row gather.  Groups
-// are sized so the units fill whole waves of one CTA per SM and are dealt in
-// snake order (later rows have longer prefixes).
+// on the 4096-row workload (18-row units) the union is 0.52 of the per-row
+// gather.  Units are sized to fill whole waves of the co-resident CTA pairs
+// and are dealt in snake order (later rows have longer prefixes).
 //
 // Duplicated selections (a caller error) keep their meaning -- a block listed
 // c times counts c times -- through a slow per-row recount.
@@ -890,16 +898,17 @@ __device__ __forceinline__ void named_arrive(int id)
 // wg + 2, ...; slot = t & 127 (row slot / G, head slot % G) is the thread's
 // TMEM lane, and the thread handles all 64 score columns of its stage.  Per
 // stage:
-//   1. the scores (two 32-column TMEM loads; the buffer is then released),
-//      masked to the blocks the slot's row attends, and their maximum;
+//   1. the scores (two 32-column TMEM loads), masked to the blocks the
+//      slot's row attends, and their maximum;
 //   2. the reference m after the previous stage, from the other group
 //      (named barrier); m grows to this stage's maximum only when that
 //      exceeds it by more than 2^8 -- O (holding every earlier stage under
 //      the old m) is then rescaled in TMEM once P V of the previous stage is
 //      done -- and goes on to the other group;
-//   3. P = 2^(x - m) as FP16 into shared memory for P V, and the group's
-//      running sum (kept under the reference the group last used and
-//      brought to the newer one whenever it changes).
+//   3. P = 2^(x - m) as FP16 over the first 32 columns of the score buffer
+//      for P V (the first 32 tokens published on their own), and the
+//      group's running sum (kept under the reference the group last used
+//      and brought to the newer one whenever it changes).
 // The scores arrive in units of the kernel's score scale sl2 > 0 (its sign
 // was folded into Q), so a masked score of -inf gives P = 0 directly.
 // At the end of the unit both groups bring their sums to the final reference,

@@ -241,7 +241,8 @@ int paged_gqa_sparse_prefill(const void* q, const void* k_cache, const void* v_c
  *                                     they are gathered).  kv_len <= 131072
  *                                     only (else PAGED_GQA_ERR_UNSUPPORTED).
  *  rows_per_group  grouped route: rows of one group, 1 .. 128 / (Hq / Hkv);
- *                  0 = sized to fill whole waves of one CTA per SM.
+ *                  0 = sized to fill whole waves of the co-resident
+ *                  pairs of CTAs (one CTA per SM, two per unit).
  * A listed block counts once per listing on both routes (duplicates are a
  * caller error; the grouped route recounts such rows on a slow path).
  */
@@ -297,9 +298,10 @@ int paged_gqa_debug_grouped_prefill_stall(const void* q, const void* k_cache, co
  * Rows per group of the grouped route for R query rows of Hq / Hkv heads on
  * the current device, given rows_per_group as passed to
  * paged_gqa_sparse_prefill_route (0 = automatic: groups sized so the units
- * fill whole waves of one CTA per SM).  Returns the count, or a negative
- * status: PAGED_GQA_ERR_SHAPE (R < 1, Hq % Hkv != 0, rows_per_group out of
- * range), PAGED_GQA_ERR_UNSUPPORTED (more than 8 query heads per KV head),
+ * fill whole waves of the co-resident CTA pairs, each pair one unit).
+ * Returns the count, or a negative status: PAGED_GQA_ERR_SHAPE (R < 1,
+ * Hq % Hkv != 0, rows_per_group out of range), PAGED_GQA_ERR_UNSUPPORTED
+ * (more than 8 query heads per KV head),
  * PAGED_GQA_ERR_CUDA (no device to query).  Host only; launches nothing.
  * The pages have no counterpart of this helper: it tells a caller how the
  * grouped route partitions its rows (for sizing benchmarks and reports).
