@@ -122,15 +122,15 @@ int prefill_route_impl(const void* q, const void* k_cache, const void* v_cache,
 // the union of a row group is much smaller than the sum of its rows'
 // selections; below that the per-row kernel is faster.  Measured on 4096
 // rows over 32768 tokens (L2 flushed before each call): FP16 rows are faster
-// grouped at every density measured, from 128 selections (0.255 vs 0.289 ms)
+// grouped at every density measured, from 16 selections (0.087 vs 0.133 ms)
 // through 512 (0.552 vs 0.820 ms) to 2048 (0.871 vs 2.974 ms):
-// 256 n_sel >= kv_len; E4M3 rows, whose per-row gather moves half the bytes
+// 2048 n_sel >= kv_len; E4M3 rows, whose per-row gather moves half the bytes
 // while the grouped route converts them to binary16 as it gathers, cross
 // over between 768 selections (0.898 vs 0.850 ms) and 1024 (0.954 vs
 // 1.103 ms), near 850: 36 n_sel >= kv_len.
 bool auto_picks_grouped(int n_sel, int kv_len, bool e4m3)
 {
-    const int64_t density = e4m3 ? 36 : 256;
+    const int64_t density = e4m3 ? 36 : 2048;
     return density * n_sel >= (int64_t)kv_len;
 }
 

@@ -225,7 +225,7 @@ int paged_gqa_sparse_prefill(const void* q, const void* k_cache, const void* v_c
  * Changes), arguments, layouts, inert rules and flags, computed by one of
  * two designs whose results agree within rounding:
  *  route = PAGED_GQA_PREFILL_AUTO     grouped when kv_len <= 131072 and
- *                                     256 * n_sel >= kv_len (FP16) or
+ *                                     2048 * n_sel >= kv_len (FP16) or
  *                                     36 * n_sel >= kv_len (E4M3): selections
  *                                     dense enough that row-group unions are
  *                                     small; per-row otherwise;

@@ -251,11 +251,11 @@ def test_binding_fails_loudly_without_library(monkeypatch):
 
 
 def test_auto_route_follows_the_documented_rule(L):
-    """PAGED_GQA_PREFILL_AUTO: grouped when 256 n_sel >= kv_len (FP16) or
+    """PAGED_GQA_PREFILL_AUTO: grouped when 2048 n_sel >= kv_len (FP16) or
     36 n_sel >= kv_len (E4M3), and the grouped route supports the shape."""
     f = L.paged_gqa_sparse_prefill_auto_route
-    assert f(4096, 6, 1, 32768, 128, 0) == 2           # FP16, 256 * 128 = 32768
-    assert f(4096, 6, 1, 32768, 127, 0) == 1
+    assert f(4096, 6, 1, 32768, 16, 0) == 2            # FP16, 2048 * 16 = 32768
+    assert f(4096, 6, 1, 32768, 15, 0) == 1
     assert f(4096, 6, 1, 32768, 911, 1) == 2           # E4M3, 36 * 911 >= 32768
     assert f(4096, 6, 1, 32768, 910, 1) == 1
     assert f(4096, 6, 1, 131076, 4096, 0) == 1         # beyond the grouped route's bitmap
