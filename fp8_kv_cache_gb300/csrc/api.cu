@@ -117,21 +117,33 @@ int prefill_route_impl(const void* q, const void* k_cache, const void* v_cache,
                        void* stream, int route, int rows_per_group, long spin_limit,
                        int stall_stage);
 
-// Automatic route choice (the grouped route must also support the shape):
-// the grouped kernel once rows select enough of the sequence's blocks that
-// the union of a row group is much smaller than the sum of its rows'
-// selections; below that the per-row kernel is faster.  Measured on 4096
-// rows over 32768 tokens (L2 flushed before each call): FP16 rows are faster
-// grouped at every density measured, from 16 selections (0.087 vs 0.133 ms)
-// through 512 (0.552 vs 0.820 ms) to 2048 (0.871 vs 2.974 ms):
-// 2048 n_sel >= kv_len; E4M3 rows, whose per-row gather moves half the bytes
-// while the grouped route converts them to binary16 as it gathers, cross
-// over between 768 selections (0.898 vs 0.850 ms) and 1024 (0.954 vs
-// 1.103 ms), near 850: 36 n_sel >= kv_len.
-bool auto_picks_grouped(int n_sel, int kv_len, bool e4m3)
+// Automatic route choice (the grouped route must also support the shape).
+// The grouped kernel pays a fixed cost per call (a unit's setup and the
+// pair exchange, ~20 us) and then gathers each row group's union of blocks
+// once; the per-row kernel gathers every row's blocks for that row alone.
+// Measured over 32768 tokens (L2 flushed before each call):
+//  * FP16, 4096 rows: grouped is faster at every density measured, from 16
+//    selections (0.087 vs 0.133 ms) through 512 (0.552 vs 0.820 ms) to 2048
+//    (0.871 vs 2.974 ms); from 1024 rows on it is faster from 16 selections
+//    (33 vs 42 us at 1024 rows);
+//  * FP16, 1 to 512 rows: per row is faster up to 128 selections (15 vs
+//    27 us at 128 rows x 16, 48 vs 52 us at 512 rows x 128), grouped from
+//    512 (46 vs 60 us at 1 row, 111 vs 128 us at 512 rows: a unit's
+//    half-tiles are split over two SMs);
+//  * E4M3, 4096 rows: the per-row gather moves half the bytes while the
+//    grouped route converts them to binary16 as it gathers; they cross over
+//    between 768 selections (0.898 vs 0.850 ms) and 1024 (0.954 vs
+//    1.103 ms), near 850; at 1 to 512 rows per row is as fast or faster
+//    through 512 selections.
+// Rule, with rows x KV heads = the per-row kernel's CTAs: FP16 grouped when
+// 64 n_sel >= kv_len, or when rows x KV heads >= 1024 and 2048 n_sel >=
+// kv_len; E4M3 grouped when rows x KV heads >= 1024 and 36 n_sel >= kv_len.
+bool auto_picks_grouped(int R, int Hkv, int n_sel, int kv_len, bool e4m3)
 {
-    const int64_t density = e4m3 ? 36 : 2048;
-    return density * n_sel >= (int64_t)kv_len;
+    const int64_t ctas = (int64_t)R * Hkv, sel = n_sel;
+    if (e4m3)
+        return ctas >= 1024 && 36 * sel >= (int64_t)kv_len;
+    return 64 * sel >= (int64_t)kv_len || (ctas >= 1024 && 2048 * sel >= (int64_t)kv_len);
 }
 
 }  // namespace
@@ -342,7 +354,7 @@ int prefill_route_impl(const void* q, const void* k_cache, const void* v_cache,
         return PAGED_GQA_ERR_SHAPE;
     const bool grouped = route == PAGED_GQA_PREFILL_GROUPED ||
                          (route == PAGED_GQA_PREFILL_AUTO && grouped_ok &&
-                          auto_picks_grouped(n_sel, kv_len, e4m3));
+                          auto_picks_grouped(R, Hkv, n_sel, kv_len, e4m3));
     const cudaError_t e =
         grouped ? launch_prefill_grouped(a, e4m3, rows_per_group, static_cast<cudaStream_t>(stream),
                                          spin_limit, stall_stage)
@@ -367,7 +379,7 @@ int paged_gqa_sparse_prefill_auto_route(int R, int Hq, int Hkv, int kv_len, int 
     a.Hkv = Hkv;
     a.G = Hq / Hkv;
     a.kv_len = kv_len;
-    return grouped_prefill_supported(a) && auto_picks_grouped(n_sel, kv_len,
+    return grouped_prefill_supported(a) && auto_picks_grouped(R, Hkv, n_sel, kv_len,
                                                                kv_dtype == PAGED_GQA_KV_E4M3)
                ? PAGED_GQA_PREFILL_GROUPED
                : PAGED_GQA_PREFILL_ROWWISE;

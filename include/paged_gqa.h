@@ -224,16 +224,19 @@ int paged_gqa_sparse_prefill(const void* q, const void* k_cache, const void* v_c
  * same operation ("[Kernel][SM70] Accelerate Qwen3.8 QSA paged prefill",
  * Changes), arguments, layouts, inert rules and flags, computed by one of
  * two designs whose results agree within rounding:
- *  route = PAGED_GQA_PREFILL_AUTO     grouped when kv_len <= 131072 and
- *                                     2048 * n_sel >= kv_len (FP16) or
- *                                     36 * n_sel >= kv_len (E4M3): selections
- *                                     dense enough that row-group unions are
- *                                     small; per-row otherwise;
+ *  route = PAGED_GQA_PREFILL_AUTO     grouped when kv_len <= 131072 and,
+ *                                     with C = R * Hkv: FP16, 64 * n_sel >=
+ *                                     kv_len, or C >= 1024 and 2048 * n_sel
+ *                                     >= kv_len; E4M3, C >= 1024 and
+ *                                     36 * n_sel >= kv_len (enough rows and
+ *                                     selections that row-group unions pay
+ *                                     for the grouped route's fixed cost);
+ *                                     per-row otherwise;
  *          PAGED_GQA_PREFILL_ROWWISE  one CTA per (row, KV head): each row's
  *                                     blocks are gathered for that row alone;
- *          PAGED_GQA_PREFILL_GROUPED  one CTA per group of consecutive rows
- *                                     of one KV head (128 query-head slots at
- *                                     most): the union of the group's blocks
+ *          PAGED_GQA_PREFILL_GROUPED  a pair of CTAs per group of consecutive
+ *                                     rows of one KV head (128 query-head
+ *                                     slots at most): the union of the group's blocks
  *                                     is gathered once into shared memory and
  *                                     each row masks the tokens it attends;
  *                                     tcgen05 tensor cores, TMEM accumulators

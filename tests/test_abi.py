@@ -251,13 +251,21 @@ def test_binding_fails_loudly_without_library(monkeypatch):
 
 
 def test_auto_route_follows_the_documented_rule(L):
-    """PAGED_GQA_PREFILL_AUTO: grouped when 2048 n_sel >= kv_len (FP16) or
-    36 n_sel >= kv_len (E4M3), and the grouped route supports the shape."""
+    """PAGED_GQA_PREFILL_AUTO, with C = R * Hkv: FP16 grouped when
+    64 n_sel >= kv_len, or C >= 1024 and 2048 n_sel >= kv_len; E4M3 grouped
+    when C >= 1024 and 36 n_sel >= kv_len; always only where the grouped
+    route supports the shape."""
     f = L.paged_gqa_sparse_prefill_auto_route
-    assert f(4096, 6, 1, 32768, 16, 0) == 2            # FP16, 2048 * 16 = 32768
+    assert f(4096, 6, 1, 32768, 16, 0) == 2            # FP16, C >= 1024, 2048 * 16 = 32768
     assert f(4096, 6, 1, 32768, 15, 0) == 1
+    assert f(1024, 6, 1, 32768, 16, 0) == 2
+    assert f(1023, 6, 1, 32768, 16, 0) == 1            # C < 1024: the dense rule only
+    assert f(512, 12, 2, 32768, 16, 0) == 2            # C = 1024 over two KV heads
+    assert f(1, 6, 1, 32768, 512, 0) == 2              # 64 * 512 = 32768
+    assert f(512, 6, 1, 32768, 511, 0) == 1
     assert f(4096, 6, 1, 32768, 911, 1) == 2           # E4M3, 36 * 911 >= 32768
     assert f(4096, 6, 1, 32768, 910, 1) == 1
+    assert f(1023, 6, 1, 32768, 4096, 1) == 1          # E4M3 needs C >= 1024
     assert f(4096, 6, 1, 131076, 4096, 0) == 1         # beyond the grouped route's bitmap
     assert f(-1, 6, 1, 32768, 512, 0) == -3
     assert f(10, 7, 2, 32768, 512, 0) == -3
