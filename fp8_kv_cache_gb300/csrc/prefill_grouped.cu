@@ -1101,16 +1101,19 @@ __device__ __forceinline__ void cluster_sync_all()
 // 128 c .. 128 c + 127; each softmax thread (slot, warpgroup wg) owns 64 of
 // them.  Step 1 (between the two cluster barriers): send the partner the
 // thread's accumulator over the partner's 64 dimensions, and (wg 0) m and l,
-// into the partner's shared memory (the first two ring slots, swizzled: the
-// ring is idle between units).  Step 2: combine the two halves,
+// into the partner's shared memory (the first two ring slots: the ring is
+// idle between units).  Step 2: combine the two halves,
 //   out = (2^(m_a - M) O_a + 2^(m_b - M) O_b) / (2^(m_a - M) l_a + 2^(m_b - M) l_b)
 // (M = max(m_a, m_b); a half with l = 0 adds nothing), and write FP16.
-// Exchange buffer: slot s's 128 floats are 32 chunks of 16 bytes at
-// 512 s + 16 (c ^ (s & 7)) bytes of the first two ring slots, so the lanes of a
-// warp (consecutive slots) spread their 16-byte accesses over all banks.
-__device__ __forceinline__ uint32_t xchg_offset(int slot, int chunk)
+// Exchange buffer (the first two ring slots): the sending warp (warpgroup
+// wg, lane quarter wq) and the combining warp of the partner are the same
+// (slot, wg) threads, so each warp has an 8 KB block, chunk-major: chunk c
+// (16 bytes, c = 0..15) of lane l at 16 (32 c + l).  For one chunk the 32
+// lanes write 512 contiguous bytes to the partner and read them back free of
+// bank conflicts.
+__device__ __forceinline__ uint32_t xchg_offset(int wg, int wq, int lane, int chunk)
 {
-    return (uint32_t)(512 * slot + 16 * (chunk ^ (slot & 7)));
+    return (uint32_t)(8192 * (4 * wg + wq) + 16 * (32 * chunk + lane));
 }
 
 __device__ void pair_send(Smem& sm, uint32_t crank, float2 ml)
@@ -1129,7 +1132,7 @@ __device__ void pair_send(Smem& sm, uint32_t crank, float2 ml)
 #pragma unroll
     for (int e = 0; e < 16; ++e)
         asm volatile("st.shared::cluster.v4.u32 [%0], {%1,%2,%3,%4};"
-                     ::"r"(rb + xchg_offset(slot, 16 * wg + e)),
+                     ::"r"(rb + xchg_offset(wg, wq, t & 31, e)),
                      "r"(have ? o[4 * e] : 0u), "r"(have ? o[4 * e + 1] : 0u),
                      "r"(have ? o[4 * e + 2] : 0u), "r"(have ? o[4 * e + 3] : 0u)
                      : "memory");
@@ -1164,7 +1167,7 @@ __device__ void pair_combine(const GroupArgs& ga, Smem& sm, int r0, int Rg, int 
         float pb[16];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            const float4 v = *reinterpret_cast<const float4*>(xb + xchg_offset(slot, 16 * wg + 4 * c + e));
+            const float4 v = *reinterpret_cast<const float4*>(xb + xchg_offset(wg, wq, t & 31, 4 * c + e));
             pb[4 * e] = v.x;
             pb[4 * e + 1] = v.y;
             pb[4 * e + 2] = v.z;
