@@ -833,13 +833,13 @@ __device__ void issue_pv(Smem& sm, Cursor& cur, int nt)
 
 // How many times block b is listed in the selection row (duplicates are a
 // caller error that still counts per listing); the own block counts once.
-__device__ int listed_count(const PrefillArgs& a, int r, int b, int own)
+__device__ int listed_count(const int32_t* sel, int n_sel, int r, int b, int own)
 {
     if (b == own)
         return 1;
-    const int32_t* row = a.sel + (size_t)r * a.n_sel;
+    const int32_t* row = sel + (size_t)r * n_sel;
     int c = 0;
-    for (int e = 0; e < a.n_sel; ++e)
+    for (int e = 0; e < n_sel; ++e)
         c += __ldg(row + e) == b;
     return c;
 }
@@ -853,20 +853,22 @@ __device__ int listed_count(const PrefillArgs& a, int r, int b, int own)
 // the stage's P (32 TMEM columns of f16 pairs at taddr, just stored) are
 // multiplied by their blocks' listing counts; returns the mass added.
 // Warp-collective (TMEM loads and stores are): lanes without duplicates
-// write their row back unchanged.
-__device__ __noinline__ float scale_listed(const PrefillArgs& a, const Smem& sm, uint32_t taddr,
-                                           bool dup, int r, int own, int nbw, int k0,
-                                           uint32_t live16)
+// write their row back unchanged.  (The selection comes by value: no
+// address of the kernel's parameters escapes into this out-of-line call.)
+__device__ __noinline__ float scale_listed(const int32_t* sel, int n_sel, const Smem& sm,
+                                           uint32_t taddr, bool dup, int r, int own, int nbw,
+                                           int k0, uint32_t live16)
 {
     uint32_t pk[32];
     tc::tmem_wait_st();                        // the stores just issued, before reading them
     tc::tmem_ld32(taddr, pk);
     tc::tmem_wait_ld();
     float added = 0.f;
-    for (int kb = 0; dup && kb < kStageBlocks; ++kb) {
-        if (!((live16 >> kb) & 1u))
+#pragma unroll
+    for (int kb = 0; kb < kStageBlocks; ++kb) {
+        if (!dup || !((live16 >> kb) & 1u))
             continue;
-        const int cnt = listed_count(a, r, block_of_rank(sm, nbw, k0 + kb), own);
+        const int cnt = listed_count(sel, n_sel, r, block_of_rank(sm, nbw, k0 + kb), own);
         if (cnt == 1)
             continue;
         for (int e = 0; e < 2; ++e) {
@@ -1044,7 +1046,7 @@ __device__ float2 softmax_unit(const GroupArgs& ga, Smem& sm, Cursor& cur, int r
         }
         l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
         if (wdup)                              // duplicated selections: count per listing
-            l += scale_listed(a, sm, tl + kTmemS + 64 * buf, dup, r0 + rl, own, nbw,
+            l += scale_listed(a.sel, a.n_sel, sm, tl + kTmemS + 64 * buf, dup, r0 + rl, own, nbw,
                               kStageBlocks * (h0 + i), live16);
 
         tc::tmem_wait_st();                    // P and any O rescale stores
