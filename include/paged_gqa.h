@@ -236,9 +236,10 @@ int paged_gqa_sparse_prefill(const void* q, const void* k_cache, const void* v_c
  *                                     blocks are gathered for that row alone;
  *          PAGED_GQA_PREFILL_GROUPED  a pair of CTAs per group of consecutive
  *                                     rows of one KV head (128 query-head
- *                                     slots at most): the union of the group's blocks
- *                                     is gathered once into shared memory and
- *                                     each row masks the tokens it attends;
+ *                                     slots at most): the union of the
+ *                                     group's blocks is gathered once into
+ *                                     shared memory (half of it by each CTA)
+ *                                     and each row masks the tokens it attends;
  *                                     tcgen05 tensor cores, TMEM accumulators
  *                                     (E4M3 rows are converted to binary16 as
  *                                     they are gathered).  kv_len <= 131072
