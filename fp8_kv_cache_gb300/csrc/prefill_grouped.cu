@@ -306,33 +306,22 @@ __device__ __forceinline__ bool staged_page_ok(const PrefillArgs& a, const int32
 __device__ __forceinline__ void union_entries(const PrefillArgs& a, Smem& sm, const int32_t* st,
                                               int c0, int n, int& flags, const int32_t* btab)
 {
-    EntryRun r(a, c0, n);
-    int cw = -1;                             // the bitmap word being gathered, its bits
-    uint32_t cb = 0u;
-    for (int own = r.i < r.i1 ? sm.row_own[r.rl] : -1; r.i < r.i1;) {
-        const int b = st[r.i];
-        if (own >= 0 && b >= 0) {
-            if (b >= own) {
-                flags |= PAGED_GQA_FLAG_BAD_SEL;
-            } else if (btab != nullptr && !staged_page_ok(a, btab, b)) {
-                flags |= PAGED_GQA_FLAG_BAD_PAGE;
-            } else {
-                if ((b >> 5) != cw) {
-                    if (cb)
-                        atomicOr(&sm.bitmap[cw], cb);
-                    cw = b >> 5;
-                    cb = 0u;
-                }
-                cb |= 1u << (b & 31);
-            }
+#pragma unroll 4
+    for (int i = threadIdx.x; i < n; i += kThreads) {
+        const int rl = (c0 + i) / a.n_sel;
+        const int own = sm.row_own[rl], b = st[i];
+        if (own < 0 || b < 0)
+            continue;
+        if (b >= own) {
+            flags |= PAGED_GQA_FLAG_BAD_SEL;
+            continue;
         }
-        const int rl = r.rl;
-        r.next(a);
-        if (r.rl != rl && r.i < r.i1)
-            own = sm.row_own[r.rl];
+        if (btab != nullptr && !staged_page_ok(a, btab, b)) {
+            flags |= PAGED_GQA_FLAG_BAD_PAGE;
+            continue;
+        }
+        atomicOr(&sm.bitmap[b >> 5], 1u << (b & 31));
     }
-    if (cb)
-        atomicOr(&sm.bitmap[cw], cb);
 }
 
 // Stage masks of half-tiles [ht0, ht0 + cap) from the staged entries of a
